@@ -1,0 +1,144 @@
+"""fp64 CPU oracle for the FlashAttention-2 forward pass.
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package; the product library
+never does, and it shares no code with the CUDA path.  The arithmetic lives
+in ``attn_ref.c`` (plain three-pass softmax attention in double precision,
+"Flash Attention 全解析(上)" section 1.2, with the per-row logsumexp of
+"FlashAttention 怎么做?online softmax 怎么更新?", FlashAttention-2 follow-up);
+this module only compiles it with gcc and marshals numpy arrays through ctypes.
+
+Parity pins (checked by the CPU test suite): the pages' worked online-softmax
+example, an independent library routine (torch's float64 CPU attention) on
+tiny shapes, closed forms (uniform weights when K = 0, a single kept key,
+causal row 0), invariants (convexity of O, LSE bounds, permutation
+invariance) and brute-force enumeration on tiny shapes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_ref.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_ref.c into liboracle.so next to it (gcc, portable flags)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    finally:
+        if os.path.exists(tmp):
+            os.remove(tmp)
+    return _LIB_PATH
+
+
+class Oracle:
+    """The oracle functions bound to one compiled copy of attn_ref.c."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        lib.oracle_attention_rows.restype = ctypes.c_int
+        lib.oracle_attention_rows.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_int,
+                                              ctypes.c_float, p, i64, p, p, ctypes.c_int]
+        lib.oracle_attention.restype = ctypes.c_int
+        lib.oracle_attention.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_int,
+                                         ctypes.c_float, p, p, ctypes.c_int]
+        self.lib = lib
+        self.path = lib_path
+
+    def attention(self, Q, K, V, causal: bool, scale: float, nthreads: int | None = None):
+        """Exact attention of every row.  Q [B,H,Nq,d], K/V [B,H,Nk,d] bf16 bits.
+
+        Returns (O [B,H,Nq,d] float64, LSE [B,H,Nq] float64).
+        """
+        Q, K, V = _bits(Q), _bits(K), _bits(V)
+        B, H, Nq, d = Q.shape
+        Nk = K.shape[2]
+        if K.shape != (B, H, Nk, d) or V.shape != K.shape:
+            raise ValueError("shape mismatch")
+        O = np.empty((B, H, Nq, d), dtype=np.float64)
+        LSE = np.empty((B, H, Nq), dtype=np.float64)
+        rc = self.lib.oracle_attention(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d,
+                                       int(bool(causal)), float(scale), _ptr(O), _ptr(LSE),
+                                       nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_attention failed with code {rc}")
+        return O, LSE
+
+    def attention_rows(self, Q, K, V, causal: bool, scale: float, rows,
+                       nthreads: int | None = None):
+        """Exact attention of selected rows.
+
+        ``rows`` holds flattened row ids (b*H + h)*Nq + i.  Returns
+        (O [len(rows), d] float64, LSE [len(rows)] float64) in the order given.
+        """
+        Q, K, V = _bits(Q), _bits(K), _bits(V)
+        B, H, Nq, d = Q.shape
+        Nk = K.shape[2]
+        if K.shape != (B, H, Nk, d) or V.shape != K.shape:
+            raise ValueError("shape mismatch")
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        n = rows.shape[0]
+        O = np.empty((n, d), dtype=np.float64)
+        LSE = np.empty((n,), dtype=np.float64)
+        rc = self.lib.oracle_attention_rows(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d,
+                                            int(bool(causal)), float(scale), _ptr(rows), n,
+                                            _ptr(O), _ptr(LSE), nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_attention_rows failed with code {rc}")
+        return O, LSE
+
+
+def compile_source(src_path: str, out_path: str) -> str:
+    """Compile a copy of the oracle source (used by the tests' planted-mistake checks)."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-o", out_path, src_path, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out_path
+
+
+def _default() -> Oracle:
+    global _lib
+    if _lib is None:
+        _lib = Oracle(build())
+    return _lib
+
+
+def _bits(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16 or a.ndim != 4:
+        raise TypeError("oracle inputs are [B,H,N,d] uint16 arrays of bf16 bit patterns")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def attention(Q, K, V, causal: bool, scale: float, nthreads: int | None = None):
+    """Exact attention of every row (see ``Oracle.attention``)."""
+    return _default().attention(Q, K, V, causal, scale, nthreads)
+
+
+def attention_rows(Q, K, V, causal: bool, scale: float, rows, nthreads: int | None = None):
+    """Exact attention of selected rows (see ``Oracle.attention_rows``)."""
+    return _default().attention_rows(Q, K, V, causal, scale, rows, nthreads)

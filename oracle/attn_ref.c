@@ -1,0 +1,186 @@
+/*
+ * fp64 CPU oracle for the FlashAttention-2 forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously correct
+ * definition that the CUDA path is checked against.  Only the tests, the
+ * package smoke check and the benchmark's CPU-baseline leg may load it.  It
+ * shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes is plain scaled-dot-product attention written as the
+ * three-pass softmax of the pages, not the tiled method:
+ *   "Flash Attention 全解析(上)", section 1.2 (标准 Attention 的三趟式计算流程):
+ *     pass 1  S = Q K^T (scaled), row max m
+ *     pass 2  l = rowsum exp(S - m)
+ *     pass 3  O = (exp(S - m) / l) V
+ *   "FlashAttention 怎么做?online softmax 怎么更新?", section "shape" and the
+ *   FlashAttention-2 follow-up question: one logsumexp per row, L = m + log l.
+ * The tiled method reaches exactly this result up to rounding order (the same
+ * page, "online softmax" paragraph: the block-wise l equals the one-shot sum).
+ *
+ * Readings taken where the pages are silent:
+ *   - inputs are bf16 bit patterns; each is widened exactly to double, so the
+ *     oracle sees the same rounded values the GPU sees;
+ *   - scale is the caller's float, widened (not recomputed as 1/sqrt(d));
+ *   - causal masking is top-left aligned: row i keeps keys j <= i (and j < Nk).
+ *     Masked keys are excluded from all three passes, so no row is ever empty
+ *     while Nk >= 1;
+ *   - logsumexp is the natural logarithm of the sum over kept keys of
+ *     exp(scaled score).
+ *
+ * Layout: Q [B,H,Nq,d], K and V [B,H,Nk,d], all contiguous (BHSD).  Outputs
+ * are double: O [rows, d] and LSE [rows].
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Exact widening of a bf16 bit pattern: bf16 is the upper half of a binary32. */
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+typedef struct {
+    const uint16_t *Q, *K, *V;
+    int64_t H, Nq, Nk, d;
+    int causal;
+    double scale;
+    const int64_t *rows;    /* flattened (b*H + h)*Nq + i; NULL = all rows */
+    int64_t nrows;
+    double *O, *LSE;        /* indexed by position in the row list */
+    int64_t next;           /* shared work counter (atomic) */
+    int error;
+} oracle_job;
+
+/* One output row, three passes over the kept keys. */
+static void attend_one_row(const oracle_job *J, int64_t flat, double *s,
+                           double *o, double *lse)
+{
+    const int64_t d = J->d;
+    const int64_t bh = flat / J->Nq;
+    const int64_t i = flat % J->Nq;
+    const uint16_t *q = J->Q + flat * d;
+    const uint16_t *kb = J->K + bh * J->Nk * d;
+    const uint16_t *vb = J->V + bh * J->Nk * d;
+
+    /* kept key set J_i: all keys, or j <= i under the causal mask */
+    int64_t n = J->Nk;
+    if (J->causal && i + 1 < n)
+        n = i + 1;
+
+    /* pass 1: scaled scores and their maximum */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            acc += bf16_bits_to_double(q[c]) * bf16_bits_to_double(kb[j * d + c]);
+        s[j] = J->scale * acc;
+        if (s[j] > m)
+            m = s[j];
+    }
+
+    /* pass 2: normaliser */
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j)
+        l += exp(s[j] - m);
+
+    /* pass 3: normalised weights times V */
+    for (int64_t c = 0; c < d; ++c)
+        o[c] = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        const double w = exp(s[j] - m) / l;
+        for (int64_t c = 0; c < d; ++c)
+            o[c] += w * bf16_bits_to_double(vb[j * d + c]);
+    }
+    *lse = m + log(l);
+}
+
+#define ORACLE_CHUNK 8
+
+static void *oracle_worker(void *arg)
+{
+    oracle_job *J = (oracle_job *)arg;
+    double *s = (double *)malloc((size_t)(J->Nk > 0 ? J->Nk : 1) * sizeof(double));
+    if (!s) {
+        __atomic_store_n(&J->error, 1, __ATOMIC_RELAXED);
+        return NULL;
+    }
+    for (;;) {
+        int64_t start = __atomic_fetch_add(&J->next, ORACLE_CHUNK, __ATOMIC_RELAXED);
+        if (start >= J->nrows)
+            break;
+        int64_t end = start + ORACLE_CHUNK < J->nrows ? start + ORACLE_CHUNK : J->nrows;
+        for (int64_t r = start; r < end; ++r) {
+            int64_t flat = J->rows ? J->rows[r] : r;
+            attend_one_row(J, flat, s, J->O + r * J->d, J->LSE + r);
+        }
+    }
+    free(s);
+    return NULL;
+}
+
+/*
+ * Attention for a list of output rows.
+ *   rows   flattened row ids (b*H + h)*Nq + i, or NULL for every row in order;
+ *   nrows  number of rows to compute (must be B*H*Nq when rows is NULL);
+ *   O      nrows*d doubles, LSE nrows doubles, written in row-list order;
+ *   nthreads  worker threads (<= 0: one).
+ * Returns 0 on success, 1 on a bad argument (including a row id out of
+ * range or Nk < 1), 2 if a worker could not allocate its score buffer.
+ */
+int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                          int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                          int causal, float scale, const int64_t *rows, int64_t nrows,
+                          double *O, double *LSE, int nthreads)
+{
+    if (!Q || !K || !V || !O || !LSE || B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || nrows < 0)
+        return 1;
+    const int64_t total = B * H * Nq;
+    if (!rows && nrows != total)
+        return 1;
+    if (rows)
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= total)
+                return 1;
+    if (nrows == 0)
+        return 0;
+
+    oracle_job J;
+    J.Q = Q; J.K = K; J.V = V;
+    J.H = H; J.Nq = Nq; J.Nk = Nk; J.d = d;
+    J.causal = causal ? 1 : 0;
+    J.scale = (double)scale;
+    J.rows = rows; J.nrows = nrows;
+    J.O = O; J.LSE = LSE;
+    J.next = 0; J.error = 0;
+
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 1024)
+        nthreads = 1024;
+    pthread_t tid[1024];
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tid[started], NULL, oracle_worker, &J) != 0)
+            break;
+        ++started;
+    }
+    oracle_worker(&J);
+    for (int t = 0; t < started; ++t)
+        pthread_join(tid[t], NULL);
+    return J.error ? 2 : 0;
+}
+
+/* Every row of every (b, h): O [B,H,Nq,d], LSE [B,H,Nq]. */
+int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                     int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                     int causal, float scale, double *O, double *LSE, int nthreads)
+{
+    return oracle_attention_rows(Q, K, V, B, H, Nq, Nk, d, causal, scale,
+                                 NULL, B * H * Nq, O, LSE, nthreads);
+}
