@@ -1,1 +1,121 @@
-"""GB300-native FlashAttention-2 forward (sm_103a)."""
+"""GB300-native FlashAttention-2 forward pass (sm_103a).
+
+Python binding of ``libfa2.so`` (C ABI in ``include/fa2.h``).  This module
+only marshals arguments: every step of the attention pass runs in the
+library's CUDA kernels.  PyTorch provides device memory and streams.  There
+is no fallback: if the library is missing or the device is unusable, calls
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+FA2_OK = 0
+FA2_ERR_NULL = 1
+FA2_ERR_ALIGN = 2
+FA2_ERR_SHAPE = 3
+FA2_ERR_HEADDIM = 4
+FA2_ERR_LAUNCH = 5
+FA2_ERR_TIMEOUT = 6
+FA2_ERR_SCALE = 7
+FA2_ERR_MEMORY = 8
+FA2_ERR_DEVICE = 9
+
+# Every function the C header declares, with its ctypes signature.
+_P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_FORWARD_ARGS = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]
+SIGNATURES = {
+    "fa2_forward": (_I, _FORWARD_ARGS),
+    "fa2_forward_simt": (_I, _FORWARD_ARGS),
+    "fa2_status_string": (ctypes.c_char_p, [_I]),
+    "fa2_device_status": (_I, [_P, _I]),
+}
+
+_lib = None
+
+
+class FA2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa2_status_string(status)} (status {status})")
+
+
+def library() -> ctypes.CDLL:
+    """Load libfa2.so (built in-tree by ``exact_attention_17_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -m exact_attention_17_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def fa2_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, stream) -> int:
+    """Raw C call: pointers (ints) and sizes, returns the status code."""
+    return library().fa2_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, int(bool(causal)), scale, stream)
+
+
+def fa2_forward_simt(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, stream) -> int:
+    """Raw C call of the CUDA-core cross-check implementation."""
+    return library().fa2_forward_simt(Q, K, V, O, LSE, B, H, Nq, Nk, d, int(bool(causal)), scale,
+                                      stream)
+
+
+def fa2_status_string(status: int) -> str:
+    return library().fa2_status_string(status).decode()
+
+
+def fa2_device_status(stream=None, reset: bool = False) -> int:
+    return library().fa2_device_status(stream, int(bool(reset)))
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+            stream=None, impl: str = "tc"):
+    """Attention forward on torch CUDA tensors.
+
+    q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; all contiguous on one device.
+    Returns (O fp32 [B,H,Nq,d], LSE fp32 [B,H,Nq]).  ``scale`` defaults to
+    1/sqrt(d) rounded to float32.  ``impl="simt"`` runs the CUDA-core
+    cross-check implementation instead of the tensor-core one.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d] matching q")
+    if scale is None:
+        scale = float(torch.tensor(d, dtype=torch.float64).rsqrt().float())
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    for name, t, shape in (("out", out, (B, H, Nq, d)), ("lse", lse, (B, H, Nq))):
+        if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous fp32 tensor of shape {shape} on {q.device}")
+    fn = {"tc": fa2_forward, "simt": fa2_forward_simt}[impl]
+    with torch.cuda.device(q.device):
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                B, H, Nq, Nk, d, causal, float(scale), _stream_handle(stream))
+    if rc != FA2_OK:
+        raise FA2Error(rc, "fa2_forward" if impl == "tc" else "fa2_forward_simt")
+    return out, lse

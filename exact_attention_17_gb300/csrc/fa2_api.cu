@@ -1,0 +1,223 @@
+// Host side of libfa2.so: argument validation, TMA tensor maps, launches.
+// The C ABI is declared (and documented) in include/fa2.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa2.h"
+#include "fa2_launch.h"
+
+namespace {
+
+// Kernels of this library OR their error bits here (one word per device).
+__device__ int g_device_status = 0;
+
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per barrier wait
+constexpr int kMaxDevices = 64;
+
+struct DriverFns {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  PFN_cuMemGetAddressRange_v3020 range = nullptr;
+  bool ok = false;
+};
+
+const DriverFns& driver() {
+  static DriverFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound;
+    cudaDriverEntryPointQueryResult q2 = cudaDriverEntryPointSymbolNotFound;
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f2, 3020, cudaEnableDefault, &q2) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess && q2 == cudaDriverEntryPointSuccess) {
+      fns.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f1);
+      fns.range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(f2);
+      fns.ok = true;
+    }
+  });
+  return fns;
+}
+
+// Per device: is it an sm_103 part, and have the kernels' shared-memory limits been raised.
+struct DeviceState {
+  std::once_flag once;
+  bool usable = false;
+};
+DeviceState g_devices[kMaxDevices];
+
+int device_ready() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA2_ERR_DEVICE;
+  DeviceState& st = g_devices[dev];
+  std::call_once(st.once, [&] {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return;
+    if (major != 10 || minor != 3) return;
+    if (fa2host::prepare_tc_d64() != cudaSuccess || fa2host::prepare_tc_d128() != cudaSuccess ||
+        fa2host::prepare_simt() != cudaSuccess)
+      return;
+    st.usable = true;
+  });
+  if (!st.usable) return FA2_ERR_DEVICE;
+  if (!driver().ok) return FA2_ERR_DEVICE;
+  return FA2_OK;
+}
+
+// The whole byte range [p, p + bytes) must be device memory of one allocation.
+bool device_range_ok(const void* p, size_t bytes) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return false;
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  if (driver().range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return false;
+  const uintptr_t begin = reinterpret_cast<uintptr_t>(p);
+  return begin >= base && bytes <= size && begin - base <= size - bytes;
+}
+
+// 3-D bf16 map over [BH][N][d]: box = 64 columns (128 B, one swizzle atom) x 128 rows x 1.
+// Rows past N read as zero instead of running into the next head.
+bool encode_map(CUtensorMap* map, const void* base, int d, int N, int BH) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = driver().encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct Problem {
+  int B, H, Nq, Nk, d;
+  long long BH;
+  bool empty;
+};
+
+int validate(const void* Q, const void* K, const void* V, const float* O, const float* LSE, int B,
+             int H, int Nq, int Nk, int d, float scale, Problem* pr) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA2_ERR_SHAPE;
+  pr->B = B; pr->H = H; pr->Nq = Nq; pr->Nk = Nk; pr->d = d;
+  pr->BH = static_cast<long long>(B) * H;
+  pr->empty = pr->BH == 0 || Nq == 0;
+  if (pr->empty) return FA2_OK;
+  if (Nk < 1) return FA2_ERR_SHAPE;
+  if (pr->BH > 0x7fffffffLL) return FA2_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA2_ERR_HEADDIM;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA2_ERR_SCALE;
+  if (!Q || !K || !V || !O || !LSE) return FA2_ERR_NULL;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                        reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O);
+  if ((a16 & 15u) != 0 || (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return FA2_ERR_ALIGN;
+  int rc = device_ready();
+  if (rc != FA2_OK) return rc;
+  const size_t bh = static_cast<size_t>(pr->BH);
+  const size_t q_elems = bh * Nq * d, kv_elems = bh * Nk * d;
+  if (!device_range_ok(Q, q_elems * 2) || !device_range_ok(K, kv_elems * 2) ||
+      !device_range_ok(V, kv_elems * 2) || !device_range_ok(O, q_elems * 4) ||
+      !device_range_ok(LSE, bh * Nq * 4))
+    return FA2_ERR_MEMORY;
+  return FA2_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" int fa2_forward(const void* Q, const void* K, const void* V, float* O, float* LSE, int B,
+                           int H, int Nq, int Nk, int d, int causal, float scale,
+                           fa2_stream_t stream) {
+  Problem pr;
+  int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr);
+  if (rc != FA2_OK || pr.empty) return rc;
+  const long long pairs = (static_cast<long long>(Nq) + 255) / 256;
+  if (pairs * pr.BH > 0x7fffffffLL) return FA2_ERR_SHAPE;
+
+  CUtensorMap mq, mk, mv;
+  if (!encode_map(&mq, Q, d, Nq, static_cast<int>(pr.BH)) ||
+      !encode_map(&mk, K, d, Nk, static_cast<int>(pr.BH)) ||
+      !encode_map(&mv, V, d, Nk, static_cast<int>(pr.BH)))
+    return FA2_ERR_SHAPE;
+
+  fa2dev::FwdParams p;
+  p.O = O;
+  p.LSE = LSE;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.BH = static_cast<int>(pr.BH);
+  p.q_pairs = static_cast<int>(pairs);
+  p.scale_log2 = scale * kLog2e;
+  p.timeout_ns = kWaitTimeoutNs;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
+    return FA2_ERR_LAUNCH;
+
+  const unsigned grid = static_cast<unsigned>(pairs * pr.BH);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = d == 64 ? fa2host::launch_tc_d64(causal != 0, mq, mk, mv, p, grid, s)
+                                : fa2host::launch_tc_d128(causal != 0, mq, mk, mv, p, grid, s);
+  return e == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
+}
+
+extern "C" int fa2_forward_simt(const void* Q, const void* K, const void* V, float* O, float* LSE,
+                                int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                fa2_stream_t stream) {
+  Problem pr;
+  int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr);
+  if (rc != FA2_OK || pr.empty) return rc;
+  if (pr.BH > 65535) return FA2_ERR_SHAPE;
+  fa2dev::SimtParams p;
+  p.Q = static_cast<const __nv_bfloat16*>(Q);
+  p.K = static_cast<const __nv_bfloat16*>(K);
+  p.V = static_cast<const __nv_bfloat16*>(V);
+  p.O = O;
+  p.LSE = LSE;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.scale_log2 = scale * kLog2e;
+  dim3 grid((Nq + fa2dev::kSimtRows - 1) / fa2dev::kSimtRows, static_cast<unsigned>(pr.BH));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = fa2host::launch_simt(d, causal != 0, p, grid, s);
+  return e == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
+}
+
+extern "C" const char* fa2_status_string(int status) {
+  switch (status) {
+    case FA2_OK: return "ok";
+    case FA2_ERR_NULL: return "a required pointer is NULL";
+    case FA2_ERR_ALIGN: return "Q/K/V/O must be 16-byte aligned and LSE 4-byte aligned";
+    case FA2_ERR_SHAPE: return "invalid or unsupported sizes";
+    case FA2_ERR_HEADDIM: return "unsupported head dimension (64 or 128)";
+    case FA2_ERR_LAUNCH: return "CUDA launch or call failed";
+    case FA2_ERR_TIMEOUT: return "a kernel gave up waiting on an internal barrier";
+    case FA2_ERR_SCALE: return "scale must be finite and > 0";
+    case FA2_ERR_MEMORY: return "a pointer is not device memory or its buffer is too small";
+    case FA2_ERR_DEVICE: return "no usable sm_103 device is current";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int fa2_device_status(fa2_stream_t stream, int reset) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA2_ERR_LAUNCH;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess) return FA2_ERR_LAUNCH;
+  if (reset) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &z, sizeof z) != cudaSuccess) return FA2_ERR_LAUNCH;
+  }
+  return v ? FA2_ERR_TIMEOUT : FA2_OK;
+}

@@ -1,0 +1,417 @@
+// FlashAttention-2 forward on the fifth-generation tensor cores (sm_103a).
+//
+// What it computes (per (b, h), per query row i):
+//   O_i = sum_j softmax_j(scale * q_i . k_j) v_j,   LSE_i = log sum_j exp(scale * q_i . k_j)
+// over the kept keys j (all keys, or j <= i with the top-left causal mask).
+//
+// How, following the FlashAttention-2 method of the pages:
+//  * loop order and grid -- "FlashAttention-2 算法架构升级" section 二 and
+//    "Flash Attention 全解析(上)" section 3.2.1: the Q block is the outer loop and
+//    owns one CTA; K/V blocks stream through the inner loop; CTAs are
+//    independent (no atomics, no inter-CTA communication);
+//  * online softmax -- "FlashAttention 怎么做?online softmax 怎么更新?",
+//    section 推导/关键公式: m' = max(m, rowmax S), P = exp(S - m'),
+//    l' = exp(m - m') l + rowsum P, O' = exp(m - m') O + P V;
+//  * lazy normalisation and the per-row logsumexp -- the same page's
+//    FlashAttention-2 question and "Flash Attention 全解析(上)" section 3.2.3:
+//    O is divided by l once after the K/V loop, L = m + log l is stored;
+//  * causal block skipping -- "FlashAttention 怎么做?", FlashAttention-2
+//    question: K/V blocks entirely above the diagonal are never visited;
+//  * tail masking -- "Triton内核实战" kernel section (masked loads for ragged N).
+//
+// GB300 mapping (not from the pages):
+//  * one CTA = two 128-row Q sub-tiles (256 query rows) sharing one K/V
+//    stream; 12 warps: warps 0-3 and 4-7 are the softmax warpgroups of
+//    sub-tile 0 and 1 (thread t owns query row t = TMEM lane t, so row max and
+//    row sum need no cross-thread reduction -- the "sliced-Q" split of
+//    "Flash Attention 全解析(上)" section 3.2.2 taken to one row per thread);
+//    warp 8 issues TMA loads, warp 9 issues tcgen05 MMAs and owns TMEM;
+//  * S = Q K^T runs as tcgen05.mma (bf16 x bf16 -> f32) from shared memory into
+//    TMEM; P is written back to TMEM as bf16 over S's columns and O += P V
+//    takes P straight from TMEM (A operand) and V from shared memory (MN-major);
+//  * TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D);
+//  * the two sub-tiles ping-pong: while one warpgroup runs its softmax the
+//    tensor core works on the other sub-tile's MMAs;
+//  * scores are scaled by scale*log2(e) inside one FMA and exponentiated with
+//    ex2; m is kept in that log2 domain and LSE converted to natural log once;
+//  * the running max used as the exponent offset is only moved when the row
+//    max grows by more than RESCALE_LOG2 (2^8): P then stays <= 256 and the
+//    correction factor exp(m - m') is applied to O and l together, so the
+//    result is the same softmax; O in TMEM is only rescaled when some row of a
+//    warp moved its offset;
+//  * every mbarrier wait is bounded; on expiry the CTA records a device error
+//    bit, unwinds, drains its copies and MMAs and frees TMEM.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx.cuh"
+
+namespace fa2dev {
+
+// Error bits OR-ed into the library's device status word.
+constexpr int kDevErrTimeout = 1;
+
+struct FwdParams {
+  float* O;        // [BH, Nq, D] fp32
+  float* LSE;      // [BH, Nq]    fp32
+  int Nq;
+  int Nk;
+  int BH;
+  int q_pairs;     // ceil(Nq / 256)
+  float scale_log2;  // scale * log2(e)
+  int* status;     // device status word
+  unsigned long long timeout_ns;
+};
+
+constexpr int kRowsPerSub = 128;   // tcgen05 M
+constexpr int kKeysPerTile = 128;  // K/V block (N of S, K of P V)
+constexpr int kThreads = 384;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct FwdConfig {
+  static constexpr int kChunks = D / 64;                    // 128-byte swizzle atoms per row
+  static constexpr uint32_t kTileBytes = kKeysPerTile * D * 2;  // one K or V tile, one Q sub-tile
+  static constexpr int kStages = D == 128 ? 4 : 8;          // K/V ring slots (K and V alternate)
+  static constexpr uint32_t kColsO0 = 256;
+  static constexpr uint32_t kColsO1 = 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSmemData = (2 + kStages) * kTileBytes;
+  static constexpr uint32_t kSmemBytes = kSmemData + 1024 /*align*/ + 1024 /*barriers*/;
+};
+
+template <int STAGES>
+struct alignas(8) FwdBarriers {
+  uint64_t q_full;
+  uint64_t kv_full[STAGES];
+  uint64_t kv_empty[STAGES];
+  uint64_t s_full[2];
+  uint64_t p_ready[2];
+  uint64_t o_done[2];
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void raise_abort(volatile int* abort, int* status) {
+  *abort = 1;
+  atomicOr(status, kDevErrTimeout);
+}
+
+// Number of K/V tiles query sub-tile `sub` of pair `u` visits (0 = no rows).
+template <bool CAUSAL>
+__device__ __forceinline__ int kv_tiles_for(int u, int sub, int Nq, int Nk) {
+  const int first = u * 2 * kRowsPerSub + sub * kRowsPerSub;
+  if (first >= Nq) return 0;
+  const int all = (Nk + kKeysPerTile - 1) / kKeysPerTile;
+  if (!CAUSAL) return all;
+  const int last = min(first + kRowsPerSub - 1, Nq - 1);
+  return min(all, last / kKeysPerTile + 1);
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa2_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using Cfg = FwdConfig<D>;
+  constexpr int STAGES = Cfg::kStages;
+  constexpr uint32_t TILE = Cfg::kTileBytes;
+  constexpr int NCH = Cfg::kChunks;
+  constexpr uint32_t kChunkBytes = kRowsPerSub * 128;  // one 64-column chunk of a 128-row tile
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;                  // two sub-tiles
+  uint8_t* sKV = smem + 2 * TILE;      // STAGES tiles
+  auto* bars = reinterpret_cast<FwdBarriers<STAGES>*>(smem + Cfg::kSmemData);
+  volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work item: (pair u of query sub-tiles, b*H + h).  Pairs of one head are
+  // adjacent so that concurrently running CTAs share K/V tiles through L2;
+  // under the causal mask the heaviest pairs of a head start first.
+  const int U = p.q_pairs;
+  const int bh = blockIdx.x / U;
+  int u = blockIdx.x - bh * U;
+  if (CAUSAL) u = U - 1 - u;
+  const int n0 = kv_tiles_for<CAUSAL>(u, 0, p.Nq, p.Nk);
+  const int n1 = kv_tiles_for<CAUSAL>(u, 1, p.Nq, p.Nk);
+  const int nmax = max(n0, n1);
+  const int q_row0 = u * 2 * kRowsPerSub;
+
+  if (threadIdx.x == 0) {
+    bar_init(&bars->q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      bar_init(&bars->kv_full[s], 1);
+      bar_init(&bars->kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      bar_init(&bars->s_full[i], 1);
+      bar_init(&bars->p_ready[i], kRowsPerSub);
+      bar_init(&bars->o_done[i], 1);
+    }
+    bar_init(&bars->mma_drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars->tmem_base, Cfg::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const uint32_t qbytes = (n0 > 0 ? TILE : 0u) + (n1 > 0 ? TILE : 0u);
+      bar_arrive_expect_tx(&bars->q_full, qbytes);
+      for (int s = 0; s < 2; ++s) {
+        if ((s == 0 ? n0 : n1) == 0) continue;
+        for (int c = 0; c < NCH; ++c)
+          tma_load_3d(sQ + s * TILE + c * kChunkBytes, &tm_q, &bars->q_full, c * 64,
+                      q_row0 + s * kRowsPerSub, bh);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < nmax && ok; ++j) {
+        for (int kind = 0; kind < 2; ++kind) {
+          const int slot = issued % STAGES;
+          const int round = issued / STAGES;
+          if (round > 0 && !wait_bar(&bars->kv_empty[slot], (round - 1) & 1, abort, p.timeout_ns)) {
+            raise_abort(abort, p.status);
+            ok = false;
+            break;
+          }
+          bar_arrive_expect_tx(&bars->kv_full[slot], TILE);
+          const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
+          for (int c = 0; c < NCH; ++c)
+            tma_load_3d(sKV + slot * TILE + c * kChunkBytes, map, &bars->kv_full[slot], c * 64,
+                        j * kKeysPerTile, bh);
+          ++issued;
+        }
+      }
+      // Before the CTA may exit, every copy it started must have landed.
+      // Only the last STAGES copies can still be in flight.
+      volatile int never = 0;
+      if (qbytes) wait_bar(&bars->q_full, 0, &never, p.timeout_ns);
+      for (int k = max(0, issued - STAGES); k < issued; ++k)
+        wait_bar(&bars->kv_full[k % STAGES], (k / STAGES) & 1, &never, p.timeout_ns);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nmax > 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(kRowsPerSub, kKeysPerTile, false, false);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(kRowsPerSub, D, false, true);
+      const uint32_t sQaddr = smem_addr(sQ);
+      const uint32_t sKVaddr = smem_addr(sKV);
+
+      // S_sub = Q_sub K^T : K-major A and B, K = D in steps of 16.
+      auto issue_s = [&](int sub, int slot) {
+        const uint32_t a0 = sQaddr + sub * TILE;
+        const uint32_t b0 = sKVaddr + slot * TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + sub * 128, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
+                 kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_sub (+)= P_sub V : P from TMEM (bf16, 2 per column), V MN-major.
+      auto issue_pv = [&](int sub, int slot, bool acc) {
+        const uint32_t b0 = sKVaddr + slot * TILE;
+        const uint32_t o = tmem + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
+#pragma unroll
+        for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
+          mma_ts(o, tmem + sub * 128 + kk * 8, sdesc_sw128(b0 + kk * 16 * 128, kChunkBytes, 1024),
+                 kIdescO, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      bool ok = wait_bar(&bars->q_full, 0, abort, p.timeout_ns);
+      // prologue: S for K tile 0
+      if (ok) ok = wait_bar(&bars->kv_full[0], 0, abort, p.timeout_ns);
+      if (ok) {
+        tc_fence_after_sync();
+        if (n0 > 0) { issue_s(0, 0); mma_commit(&bars->s_full[0]); }
+        if (n1 > 0) { issue_s(1, 0); mma_commit(&bars->s_full[1]); }
+        mma_commit(&bars->kv_empty[0]);
+      }
+      for (int j = 0; j < nmax && ok; ++j) {
+        const int iv = 2 * j + 1, ik = 2 * j + 2;
+        const int slot_v = iv % STAGES, slot_k = ik % STAGES;
+        const bool next = j + 1 < nmax;
+        if (!wait_bar(&bars->kv_full[slot_v], (iv / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
+        if (j < n0) {
+          if (!wait_bar(&bars->p_ready[0], j & 1, abort, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after_sync();
+          issue_pv(0, slot_v, j > 0);
+          mma_commit(&bars->o_done[0]);
+        }
+        if (next) {
+          if (!wait_bar(&bars->kv_full[slot_k], (ik / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after_sync();
+          if (j + 1 < n0) { issue_s(0, slot_k); mma_commit(&bars->s_full[0]); }
+        }
+        if (j < n1) {
+          if (!wait_bar(&bars->p_ready[1], j & 1, abort, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after_sync();
+          issue_pv(1, slot_v, j > 0);
+          mma_commit(&bars->o_done[1]);
+        }
+        mma_commit(&bars->kv_empty[slot_v]);
+        if (next) {
+          if (j + 1 < n1) { issue_s(1, slot_k); mma_commit(&bars->s_full[1]); }
+          mma_commit(&bars->kv_empty[slot_k]);
+        }
+      }
+      if (!ok) raise_abort(abort, p.status);
+      // Every MMA must be complete before TMEM is released.
+      mma_commit(&bars->mma_drain);
+      volatile int never = 0;
+      wait_bar(&bars->mma_drain, 0, &never, p.timeout_ns);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int sub = warp >> 2;
+    const int n_tiles = sub == 0 ? n0 : n1;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;                       // TMEM lane = row of the sub-tile
+    const int sub_row0 = q_row0 + sub * kRowsPerSub;
+    const int qi = sub_row0 + row;                        // query index within (b, h)
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + sub * 128;
+    const uint32_t tO = tmem + lane_bits + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
+    const float sl2 = p.scale_log2;
+
+    float m = -INFINITY;  // running max (log2 domain) used as the exponent offset
+    float l = 0.f;        // running sum of 2^(t - m)
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      // all lanes must agree before the warp-collective TMEM accesses
+      if (!__all_sync(0xffffffffu, wait_bar(&bars->s_full[sub], j & 1, abort, p.timeout_ns))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+
+      // masks: keys past the end, and keys after the query under the causal mask
+      const int key0 = j * kKeysPerTile;
+      const bool tail = key0 + kKeysPerTile > p.Nk;
+      const bool diag = CAUSAL && key0 + kKeysPerTile - 1 > sub_row0;
+      if (tail || diag) {
+        const int lim = CAUSAL ? min(p.Nk, qi + 1) : p.Nk;  // keys [0, lim) are kept
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (key0 + c * 32 + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
+      }
+
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+      const float m_cand = fmaxf(m, mx * sl2);
+      const bool move = (j == 0) || (m_cand > m + kRescaleLog2);
+      const float m_new = move ? m_cand : m;
+      // correction factor exp(m - m'): 0 on the first tile, exactly 1 when the offset stays
+      const float alpha = !move ? 1.f : (m == -INFINITY ? 0.f : ex2_approx(m - m_new));
+      const float off = m_new == -INFINITY ? 0.f : m_new;
+
+      float rs = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][e]), sl2, -off));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][e + 1]), sl2, -off));
+          rs += p0 + p1;
+          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+        }
+      l = l * alpha + rs;
+      m = m_new;
+      tmem_st32(tS, pk[0]);
+      tmem_st32(tS + 32, pk[1]);
+
+      // correction of the running output when some row of this warp moved its offset
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!__all_sync(0xffffffffu, wait_bar(&bars->o_done[sub], (j - 1) & 1, abort, p.timeout_ns))) {
+          ok = false;
+        }
+        else {
+          tc_fence_after_sync();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      bar_arrive(&bars->p_ready[sub]);
+      if (!ok) break;
+    }
+
+    if (n_tiles > 0 && ok) {
+      if (!__all_sync(0xffffffffu,
+                      wait_bar(&bars->o_done[sub], (n_tiles - 1) & 1, abort, p.timeout_ns))) {
+        ok = false;
+      } else {
+        tc_fence_after_sync();
+        const float inv_l = 1.f / l;
+        const bool store = qi < p.Nq;
+        float* orow = p.O + (static_cast<size_t>(bh) * p.Nq + qi) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+          if (store) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              float4 v = make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
+                                     __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+              *reinterpret_cast<float4*>(orow + c * 32 + e) = v;
+            }
+          }
+        }
+        if (store) p.LSE[static_cast<size_t>(bh) * p.Nq + qi] = (m + __log2f(l)) * 0.69314718055994531f;
+      }
+    }
+    if (!ok) raise_abort(abort, p.status);
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace fa2dev

@@ -1,0 +1,26 @@
+// Internal: launch entry points of the kernel translation units.  Each .cu
+// file instantiates one family of kernels so that they compile in parallel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa2_fwd_simt.cuh"
+#include "fa2_fwd_sm103.cuh"
+
+namespace fa2host {
+
+// Raise the dynamic shared-memory limit of every kernel in the unit (current device).
+cudaError_t prepare_tc_d64();
+cudaError_t prepare_tc_d128();
+cudaError_t prepare_simt();
+
+cudaError_t launch_tc_d64(bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const fa2dev::FwdParams& p, unsigned grid,
+                          cudaStream_t s);
+cudaError_t launch_tc_d128(bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, const fa2dev::FwdParams& p, unsigned grid,
+                           cudaStream_t s);
+cudaError_t launch_simt(int d, bool causal, const fa2dev::SimtParams& p, dim3 grid, cudaStream_t s);
+
+}  // namespace fa2host

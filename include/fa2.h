@@ -1,0 +1,101 @@
+/*
+ * fa2.h -- C ABI of libfa2.so, a FlashAttention-2 forward pass for GB300
+ * (sm_103a).
+ *
+ * The operation (per batch b, head h and query row i):
+ *
+ *     s_ij   = scale * sum_c Q[b,h,i,c] * K[b,h,j,c]
+ *     O[b,h,i,:] = sum_{j in J_i} softmax_{j in J_i}(s_ij) * V[b,h,j,:]
+ *     LSE[b,h,i] = log sum_{j in J_i} exp(s_ij)           (natural log)
+ *
+ * with J_i = {0 .. Nk-1}, or {j : j <= i} when causal (top-left aligned:
+ * query i sees keys 0..i, so no row is ever empty).  This is exact
+ * scaled-dot-product attention computed the FlashAttention-2 way: Q blocks in
+ * the outer loop (one thread block each), K/V blocks streamed in the inner
+ * loop with an online softmax (running max m and sum l, correction by
+ * exp(m_old - m_new)), normalisation once after the loop, and the per-row
+ * logsumexp L = m + log l as a second output.  Sources: "FlashAttention 怎么做?
+ * online softmax 怎么更新?" (sections 推导/关键公式 and the FlashAttention-2
+ * question), "FlashAttention-2 算法架构升级" (sections 一 and 二),
+ * "Flash Attention 全解析(上)" (sections 1.2 and 3.2), and the host wrapper of
+ * "Triton内核实战" (separate query and key lengths, an fp32 [B,H,Lq] side
+ * buffer for the row statistic).
+ *
+ * Memory and ownership.  All tensor arguments are DEVICE pointers owned by
+ * the caller; the library never allocates, frees or keeps them.  Layouts are
+ * dense row-major BHSD:
+ *     Q   bf16  [B, H, Nq, d]      K, V  bf16  [B, H, Nk, d]
+ *     O   fp32  [B, H, Nq, d]      LSE   fp32  [B, H, Nq]
+ * Q, K, V and O must be 16-byte aligned, LSE 4-byte aligned.  O and LSE are
+ * fully overwritten; no other memory is written.  The library keeps no state
+ * between calls apart from a per-device status word (fa2_device_status).
+ *
+ * Errors.  Calls are asynchronous on `stream`.  The return value reports
+ * argument errors (found on the host before anything is launched; nothing is
+ * written then) and launch errors.  A kernel that gives up waiting on one of
+ * its internal barriers (about 2 s) returns early, leaves its outputs
+ * incomplete and sets the device status word, which fa2_device_status reads.
+ */
+#ifndef FA2_H
+#define FA2_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *fa2_stream_t;
+
+typedef enum {
+  FA2_OK = 0,
+  FA2_ERR_NULL = 1,     /* a required pointer is NULL */
+  FA2_ERR_ALIGN = 2,    /* Q/K/V/O not 16-byte aligned, or LSE not 4-byte aligned */
+  FA2_ERR_SHAPE = 3,    /* negative size, Nk < 1 with rows to compute, or a size past the limits */
+  FA2_ERR_HEADDIM = 4,  /* d not supported (64 or 128) */
+  FA2_ERR_LAUNCH = 5,   /* the CUDA launch or a CUDA call failed */
+  FA2_ERR_TIMEOUT = 6,  /* a kernel gave up waiting on an internal barrier */
+  FA2_ERR_SCALE = 7,    /* scale not finite and > 0 */
+  FA2_ERR_MEMORY = 8,   /* a pointer is not device memory, or its buffer is too small */
+  FA2_ERR_DEVICE = 9    /* no usable sm_103 device is current */
+} fa2_status;
+
+/*
+ * FlashAttention-2 forward on the tensor cores (tcgen05 MMAs accumulating in
+ * tensor memory, TMA-fed K/V pipeline).
+ *   Q, K, V   device bf16 inputs (layouts above)
+ *   O, LSE    device fp32 outputs
+ *   B, H      batch and head counts (B*H <= 2^31-1)
+ *   Nq, Nk    query and key lengths (may differ; Nk >= 1 when B*H*Nq > 0)
+ *   d         head dimension, 64 or 128
+ *   causal    nonzero: mask keys j > i
+ *   scale     score scale, finite and > 0 (usually 1/sqrt(d))
+ *   stream    CUDA stream (NULL = legacy default stream)
+ * B*H*Nq == 0 is a valid empty problem: nothing is launched, FA2_OK.
+ */
+int fa2_forward(const void *Q, const void *K, const void *V, float *O, float *LSE, int B, int H,
+                int Nq, int Nk, int d, int causal, float scale, fa2_stream_t stream);
+
+/*
+ * The same operation on the CUDA cores, fp32 arithmetic, one thread per query
+ * row.  A plain second implementation used to cross-check fa2_forward on the
+ * device; slow.  Same arguments, limits and errors, plus B*H <= 65535.
+ */
+int fa2_forward_simt(const void *Q, const void *K, const void *V, float *O, float *LSE, int B,
+                     int H, int Nq, int Nk, int d, int causal, float scale, fa2_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char *fa2_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reports whether any kernel of this library on
+ * the current device has set its device status word since the last reset:
+ * FA2_OK, FA2_ERR_TIMEOUT, or FA2_ERR_LAUNCH if the synchronisation itself
+ * failed.  reset != 0 clears the word afterwards.
+ */
+int fa2_device_status(fa2_stream_t stream, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA2_H */

@@ -1,0 +1,83 @@
+"""The C ABI: the library builds for sm_103a, exports every declared symbol,
+and rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_17_gb300 as fa2
+from exact_attention_17_gb300 import build as libbuild
+
+HEADER = os.path.join(libbuild.INCLUDE, "fa2.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return fa2.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa2_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert "fa2_forward" in names and "fa2_status_string" in names
+    assert set(names) == set(fa2.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = fa2.fa2_status_string(code)
+        assert s and s != "unknown status"
+    assert fa2.fa2_status_string(12345) == "unknown status"
+
+
+def call(**kw):
+    args = dict(Q=16, K=16, V=16, O=16, LSE=16, B=1, H=1, Nq=8, Nk=8, d=64, causal=0,
+                scale=0.125, stream=None)
+    args.update(kw)
+    return fa2.fa2_forward(args["Q"], args["K"], args["V"], args["O"], args["LSE"], args["B"],
+                           args["H"], args["Nq"], args["Nk"], args["d"], args["causal"],
+                           args["scale"], args["stream"])
+
+
+@pytest.mark.parametrize("fn", ["fa2_forward", "fa2_forward_simt"])
+def test_host_side_argument_errors(lib, fn):
+    f = getattr(fa2, fn)
+
+    def c(**kw):
+        a = dict(Q=16, K=16, V=16, O=16, LSE=16, B=1, H=1, Nq=8, Nk=8, d=64, causal=0,
+                 scale=0.125, stream=None)
+        a.update(kw)
+        return f(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["Nq"], a["Nk"],
+                 a["d"], a["causal"], a["scale"], a["stream"])
+
+    # empty problems are valid and launch nothing
+    assert c(B=0) == fa2.FA2_OK
+    assert c(H=0, Q=None) == fa2.FA2_OK
+    assert c(Nq=0) == fa2.FA2_OK
+    # sizes
+    assert c(B=-1) == fa2.FA2_ERR_SHAPE
+    assert c(Nk=-1) == fa2.FA2_ERR_SHAPE
+    assert c(Nk=0) == fa2.FA2_ERR_SHAPE
+    assert c(B=1 << 16, H=1 << 16) == fa2.FA2_ERR_SHAPE
+    for d in (0, 32, 96, 256):
+        assert c(d=d) == fa2.FA2_ERR_HEADDIM
+    for s in (0.0, -1.0, float("inf"), float("nan")):
+        assert c(scale=s) == fa2.FA2_ERR_SCALE
+    for name in ("Q", "K", "V", "O", "LSE"):
+        assert c(**{name: None}) == fa2.FA2_ERR_NULL
+    for name in ("Q", "K", "V", "O"):
+        assert c(**{name: 24}) == fa2.FA2_ERR_ALIGN
+    assert c(LSE=18) == fa2.FA2_ERR_ALIGN
