@@ -1,0 +1,418 @@
+"""Benchmark of the FlashAttention-2 forward pass on GB300.
+
+One step = one forward pass (the whole hot path: tile loads, S = Q K^T,
+masking, online softmax, P V, normalisation, LSE) over one batch of seeded
+synthetic bf16 inputs already resident in HBM.  The default workload is
+B=1, H=32, Nq=Nk=16384, d=128, causal -- the head count, head dimension and
+long-sequence regime of the FlashAttention-2 utilisation table in
+"FlashAttention-2 算法架构升级" (section 四).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                        [--impl reference]
+For N > 1 launch one process per GPU with torch.distributed.run; every rank
+runs an independent replica (the pass has no exchange step) and rank 0
+prints one JSON line with the whole-job throughput.
+
+``--impl reference`` times the fp64 CPU oracle on this arm's workload (a
+bounded row sample per step) on the host cores and prints the same JSON
+line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from exact_attention_17_gb300 import inputs  # noqa: E402
+
+METRIC = "FA2 fwd TFLOP/s (causal-halved) and % of GB300 dense-BF16 tensor peak"
+DEFAULT_WORKLOAD = "b1_h32_n16384_d128_causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["exact_attention_17_gb300/csrc/fa2_fwd_sm103.cuh",
+                  "exact_attention_17_gb300/csrc/ptx.cuh",
+                  "exact_attention_17_gb300/csrc/fa2_tc_d128.cu",
+                  "exact_attention_17_gb300/csrc/fa2_tc_d64.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_bytes(w) -> float:
+    """Q, K, V read once as bf16; O and LSE written once as fp32."""
+    return w.B * w.H * (2.0 * w.Nq * w.d + 4.0 * w.Nk * w.d + 4.0 * w.Nq * w.d + 4.0 * w.Nq)
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples taken during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if self.proc is None or not self.lines:
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle (CPU) timing
+
+def oracle_sample_rate(w, Q, K, V, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on random rows of the workload for about budget_s.
+
+    Returns (TFLOP/s, cores, rows, seconds); FLOPs per row are the algorithmic
+    4 * |J_i| * d of that row (|J_i| = kept keys)."""
+    import oracle
+
+    qb, kb, vb = (inputs.bf16_bits(t) for t in (Q, K, V))
+    cores = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+    total_rows = w.B * w.H * w.Nq
+    flops = 0.0
+    rows_done = 0
+    batch = max(cores, 16)
+    t0 = time.perf_counter()
+    while True:
+        rows = rng.integers(0, total_rows, size=batch)
+        oracle.attention_rows(qb, kb, vb, w.causal, w.scale, rows, nthreads=cores)
+        i = rows % w.Nq
+        kept = np.minimum(i + 1, w.Nk) if w.causal else np.full_like(i, w.Nk)
+        flops += float(np.sum(4.0 * kept * w.d))
+        rows_done += batch
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+        batch = int(min(batch * 2, max(batch, rows_done * (budget_s - el) / max(el, 1e-3))))
+        batch = max(batch, cores)
+    return flops / el / 1e12, cores, rows_done, el
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    Q, K, V = inputs.workload_inputs(w)
+    per_step = []
+    rows_total = 0
+    cores = 0
+    for s in range(args.warmup + args.steps):
+        budget = 1.0 if s < args.warmup else args.reference_step_s
+        tf, cores, rows, el = oracle_sample_rate(w, Q, K, V, budget, seed=s)
+        if s >= args.warmup:
+            per_step.append((tf, rows, el))
+            rows_total += rows
+    secs = sum(e for _, _, e in per_step)
+    value = sum(tf * e for tf, _, e in per_step) / secs
+    sample = (f"{rows_total} uniformly drawn query rows of {w.name} over {args.steps} steps "
+              f"(~{args.reference_step_s:.0f} s each), fp64 three-pass oracle, FLOPs = 4*|J_i|*d per row")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1000 * secs / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, "oracle on host cores"),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, l2_note):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+            "causal": w.causal, "scale": w.scale, "qk_dist": f"{w.qk_dist}(std {w.qk_std})",
+            "v_dist": w.v_dist, "seed": w.seed, "inputs": "bf16 BHSD", "outputs": "fp32 O, fp32 LSE",
+            "l2": l2_note, "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-baseline-s", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline field (0 = skip)")
+    ap.add_argument("--reference-step-s", type=float, default=None,
+                    help="oracle seconds per reference step (default: ~120 s over all steps)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the workload's head count (smaller profiling captures)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    w = inputs.workload(args.workload)
+    if args.heads is not None:
+        import dataclasses
+        w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_heads{args.heads}")
+    if args.reference_step_s is None:
+        args.reference_step_s = max(1.0, min(10.0, 120.0 / max(1, args.steps)))
+
+    if args.impl == "reference":
+        return run_reference(args, w)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import exact_attention_17_gb300 as fa2
+
+    # seeded inputs, generated on the host (same bits the oracle sees)
+    Qh, Kh, Vh = inputs.workload_inputs(w)
+    Q, K, V = Qh.to(dev), Kh.to(dev), Vh.to(dev)
+    O = torch.empty(w.B, w.H, w.Nq, w.d, device=dev)
+    L = torch.empty(w.B, w.H, w.Nq, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    in_bytes = (Q.numel() + K.numel() + V.numel()) * 2
+    l2_bytes = 129 * 1024 * 1024
+    flush = None
+    if in_bytes <= 2 * l2_bytes:
+        flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+        l2_note = "L2 flushed between steps (256 MiB write, outside the kernel events)"
+    else:
+        l2_note = f"inputs {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"
+
+    def step(s):
+        fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, out=O, lse=L, stream=s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(stream)
+    torch.cuda.synchronize(dev)
+    if fa2.fa2_device_status(None, reset=True) != fa2.FA2_OK:
+        raise SystemExit("device status error during warm-up")
+
+    # timed region: K steps, per-launch events on the launching stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        with torch.cuda.stream(stream):
+            t_begin.record(stream)
+            for i in range(args.steps):
+                if flush is not None:
+                    flush.zero_()
+                starts[i].record(stream)
+                step(stream)
+                ends[i].record(stream)
+            t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    status = fa2.fa2_device_status(None, reset=True)
+    if status != fa2.FA2_OK:
+        raise SystemExit(f"device status error in the timed region: {status}")
+    launch_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    kernel_ms = sum(launch_ms)
+    total_ms = t_begin.elapsed_time(t_end)
+    timed_ms = kernel_ms if flush is not None else total_ms
+    t = torch.tensor([timed_ms], device=dev, dtype=torch.float64)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    job_ms = float(t.item())
+
+    # end to end through the public call: pinned host inputs -> device -> forward -> host result
+    Qp, Kp, Vp = Qh.pin_memory(), Kh.pin_memory(), Vh.pin_memory()
+    Op = torch.empty(O.shape, dtype=torch.float32).pin_memory()
+    Lp = torch.empty(L.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        Q.copy_(Qp, non_blocking=True)
+        K.copy_(Kp, non_blocking=True)
+        V.copy_(Vp, non_blocking=True)
+        fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, out=O, lse=L, stream=stream)
+        Op.copy_(O, non_blocking=True)
+        Lp.copy_(L, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    te = torch.tensor([e0.elapsed_time(e1)], device=dev, dtype=torch.float64)
+    if dist:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_ms = float(te.item())
+    h2d = (Qp.numel() + Kp.numel() + Vp.numel()) * 2
+    d2h = (Op.numel() + Lp.numel()) * 4
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    mean_launch_ms = statistics.mean(launch_ms)
+    achieved = w.flops / (mean_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    value = w.flops * args.steps * world / (job_ms * 1e-3) / 1e12
+    traffic = recorded_traffic(w.name)
+
+    cpu = None
+    if args.cpu_baseline_s > 0:
+        tf, cores, rows, el = oracle_sample_rate(w, Qh, Kh, Vh, args.cpu_baseline_s)
+        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{rows} uniformly drawn query rows of {w.name} in {el:.1f} s "
+                         f"(fp64 three-pass oracle, FLOPs = 4*|J_i|*d per row)"}
+
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(job_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": workload_config(w, l2_note),
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "peak_kind": f"bf16 dense burst ({peak_src})",
+            "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4),
+            "kernel": "fa2dev::fa2_fwd_tc_kernel",
+            "flops_per_launch": w.flops,
+            "algorithmic_bytes_per_launch": algorithmic_bytes(w),
+            "mean_launch_ms": round(mean_launch_ms, 4),
+        },
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(w.flops * args.e2e_steps * world / (e2e_ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -68,6 +68,13 @@ struct FwdParams {
 constexpr int kRowsPerSub = 128;   // tcgen05 M
 constexpr int kKeysPerTile = 128;  // K/V block (N of S, K of P V)
 constexpr int kThreads = 384;
+// Register budgets after the start-up rebalancing: 168 per thread at launch
+// (65536 / 384, rounded down to a multiple of 8) = 64512 in total;
+// 2 x 128 x kRegsSoftmax + 128 x kRegsProducer = 63488 stays within it.
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsProducer = 64;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsProducer <= 168 * kThreads,
+              "register rebalancing exceeds the launch allocation");
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
@@ -169,120 +176,126 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      const uint32_t qbytes = (n0 > 0 ? TILE : 0u) + (n1 > 0 ? TILE : 0u);
-      bar_arrive_expect_tx(&bars->q_full, qbytes);
-      for (int s = 0; s < 2; ++s) {
-        if ((s == 0 ? n0 : n1) == 0) continue;
-        for (int c = 0; c < NCH; ++c)
-          tma_load_3d(sQ + s * TILE + c * kChunkBytes, &tm_q, &bars->q_full, c * 64,
-                      q_row0 + s * kRowsPerSub, bh);
-      }
-      int issued = 0;
-      bool ok = true;
-      for (int j = 0; j < nmax && ok; ++j) {
-        for (int kind = 0; kind < 2; ++kind) {
-          const int slot = issued % STAGES;
-          const int round = issued / STAGES;
-          if (round > 0 && !wait_bar(&bars->kv_empty[slot], (round - 1) & 1, abort, p.timeout_ns)) {
-            raise_abort(abort, p.status);
-            ok = false;
-            break;
-          }
-          bar_arrive_expect_tx(&bars->kv_full[slot], TILE);
-          const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
+  // Each role branch starts with its register budget change, so that the
+  // compiler can allocate each branch for its own budget.
+  if (warp >= 8) {
+    regs_decrease<kRegsProducer>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        const uint32_t qbytes = (n0 > 0 ? TILE : 0u) + (n1 > 0 ? TILE : 0u);
+        bar_arrive_expect_tx(&bars->q_full, qbytes);
+        for (int s = 0; s < 2; ++s) {
+          if ((s == 0 ? n0 : n1) == 0) continue;
           for (int c = 0; c < NCH; ++c)
-            tma_load_3d(sKV + slot * TILE + c * kChunkBytes, map, &bars->kv_full[slot], c * 64,
-                        j * kKeysPerTile, bh);
-          ++issued;
+            tma_load_3d(sQ + s * TILE + c * kChunkBytes, &tm_q, &bars->q_full, c * 64,
+                        q_row0 + s * kRowsPerSub, bh);
         }
+        int issued = 0;
+        bool ok = true;
+        for (int j = 0; j < nmax && ok; ++j) {
+          for (int kind = 0; kind < 2; ++kind) {
+            const int slot = issued % STAGES;
+            const int round = issued / STAGES;
+            if (round > 0 && !wait_bar(&bars->kv_empty[slot], (round - 1) & 1, abort, p.timeout_ns)) {
+              raise_abort(abort, p.status);
+              ok = false;
+              break;
+            }
+            bar_arrive_expect_tx(&bars->kv_full[slot], TILE);
+            const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
+            for (int c = 0; c < NCH; ++c)
+              tma_load_3d(sKV + slot * TILE + c * kChunkBytes, map, &bars->kv_full[slot], c * 64,
+                          j * kKeysPerTile, bh);
+            ++issued;
+          }
+        }
+        // Before the CTA may exit, every copy it started must have landed.
+        // Only the last STAGES copies can still be in flight.
+        volatile int never = 0;
+        if (qbytes) wait_bar(&bars->q_full, 0, &never, p.timeout_ns);
+        for (int k = max(0, issued - STAGES); k < issued; ++k)
+          wait_bar(&bars->kv_full[k % STAGES], (k / STAGES) & 1, &never, p.timeout_ns);
       }
-      // Before the CTA may exit, every copy it started must have landed.
-      // Only the last STAGES copies can still be in flight.
-      volatile int never = 0;
-      if (qbytes) wait_bar(&bars->q_full, 0, &never, p.timeout_ns);
-      for (int k = max(0, issued - STAGES); k < issued; ++k)
-        wait_bar(&bars->kv_full[k % STAGES], (k / STAGES) & 1, &never, p.timeout_ns);
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nmax > 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(kRowsPerSub, kKeysPerTile, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(kRowsPerSub, D, false, true);
-      const uint32_t sQaddr = smem_addr(sQ);
-      const uint32_t sKVaddr = smem_addr(sKV);
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0 && nmax > 0) {
+        constexpr uint32_t kIdescS = idesc_bf16_f32(kRowsPerSub, kKeysPerTile, false, false);
+        constexpr uint32_t kIdescO = idesc_bf16_f32(kRowsPerSub, D, false, true);
+        const uint32_t sQaddr = smem_addr(sQ);
+        const uint32_t sKVaddr = smem_addr(sKV);
 
-      // S_sub = Q_sub K^T : K-major A and B, K = D in steps of 16.
-      auto issue_s = [&](int sub, int slot) {
-        const uint32_t a0 = sQaddr + sub * TILE;
-        const uint32_t b0 = sKVaddr + slot * TILE;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + sub * 128, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
-                 kIdescS, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_sub (+)= P_sub V : P from TMEM (bf16, 2 per column), V MN-major.
-      auto issue_pv = [&](int sub, int slot, bool acc) {
-        const uint32_t b0 = sKVaddr + slot * TILE;
-        const uint32_t o = tmem + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
-#pragma unroll
-        for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
-          mma_ts(o, tmem + sub * 128 + kk * 8, sdesc_sw128(b0 + kk * 16 * 128, kChunkBytes, 1024),
-                 kIdescO, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
+        // S_sub = Q_sub K^T : K-major A and B, K = D in steps of 16.
+        auto issue_s = [&](int sub, int slot) {
+          const uint32_t a0 = sQaddr + sub * TILE;
+          const uint32_t b0 = sKVaddr + slot * TILE;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            mma_ss(tmem + sub * 128, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
+                   kIdescS, kk > 0 ? 1u : 0u);
+          }
+        };
+        // O_sub (+)= P_sub V : P from TMEM (bf16, 2 per column), V MN-major.
+        auto issue_pv = [&](int sub, int slot, bool acc) {
+          const uint32_t b0 = sKVaddr + slot * TILE;
+          const uint32_t o = tmem + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
+  #pragma unroll
+          for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
+            mma_ts(o, tmem + sub * 128 + kk * 8, sdesc_sw128(b0 + kk * 16 * 128, kChunkBytes, 1024),
+                   kIdescO, (acc || kk > 0) ? 1u : 0u);
+          }
+        };
 
-      bool ok = wait_bar(&bars->q_full, 0, abort, p.timeout_ns);
-      // prologue: S for K tile 0
-      if (ok) ok = wait_bar(&bars->kv_full[0], 0, abort, p.timeout_ns);
-      if (ok) {
-        tc_fence_after_sync();
-        if (n0 > 0) { issue_s(0, 0); mma_commit(&bars->s_full[0]); }
-        if (n1 > 0) { issue_s(1, 0); mma_commit(&bars->s_full[1]); }
-        mma_commit(&bars->kv_empty[0]);
+        bool ok = wait_bar(&bars->q_full, 0, abort, p.timeout_ns);
+        // prologue: S for K tile 0
+        if (ok) ok = wait_bar(&bars->kv_full[0], 0, abort, p.timeout_ns);
+        if (ok) {
+          tc_fence_after_sync();
+          if (n0 > 0) { issue_s(0, 0); mma_commit(&bars->s_full[0]); }
+          if (n1 > 0) { issue_s(1, 0); mma_commit(&bars->s_full[1]); }
+          mma_commit(&bars->kv_empty[0]);
+        }
+        for (int j = 0; j < nmax && ok; ++j) {
+          const int iv = 2 * j + 1, ik = 2 * j + 2;
+          const int slot_v = iv % STAGES, slot_k = ik % STAGES;
+          const bool next = j + 1 < nmax;
+          if (!wait_bar(&bars->kv_full[slot_v], (iv / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
+          if (j < n0) {
+            if (!wait_bar(&bars->p_ready[0], j & 1, abort, p.timeout_ns)) { ok = false; break; }
+            tc_fence_after_sync();
+            issue_pv(0, slot_v, j > 0);
+            mma_commit(&bars->o_done[0]);
+          }
+          if (next) {
+            if (!wait_bar(&bars->kv_full[slot_k], (ik / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
+            tc_fence_after_sync();
+            if (j + 1 < n0) { issue_s(0, slot_k); mma_commit(&bars->s_full[0]); }
+          }
+          if (j < n1) {
+            if (!wait_bar(&bars->p_ready[1], j & 1, abort, p.timeout_ns)) { ok = false; break; }
+            tc_fence_after_sync();
+            issue_pv(1, slot_v, j > 0);
+            mma_commit(&bars->o_done[1]);
+          }
+          mma_commit(&bars->kv_empty[slot_v]);
+          if (next) {
+            if (j + 1 < n1) { issue_s(1, slot_k); mma_commit(&bars->s_full[1]); }
+            mma_commit(&bars->kv_empty[slot_k]);
+          }
+        }
+        if (!ok) raise_abort(abort, p.status);
+        // Every MMA must be complete before TMEM is released.
+        mma_commit(&bars->mma_drain);
+        volatile int never = 0;
+        wait_bar(&bars->mma_drain, 0, &never, p.timeout_ns);
       }
-      for (int j = 0; j < nmax && ok; ++j) {
-        const int iv = 2 * j + 1, ik = 2 * j + 2;
-        const int slot_v = iv % STAGES, slot_k = ik % STAGES;
-        const bool next = j + 1 < nmax;
-        if (!wait_bar(&bars->kv_full[slot_v], (iv / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
-        if (j < n0) {
-          if (!wait_bar(&bars->p_ready[0], j & 1, abort, p.timeout_ns)) { ok = false; break; }
-          tc_fence_after_sync();
-          issue_pv(0, slot_v, j > 0);
-          mma_commit(&bars->o_done[0]);
-        }
-        if (next) {
-          if (!wait_bar(&bars->kv_full[slot_k], (ik / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
-          tc_fence_after_sync();
-          if (j + 1 < n0) { issue_s(0, slot_k); mma_commit(&bars->s_full[0]); }
-        }
-        if (j < n1) {
-          if (!wait_bar(&bars->p_ready[1], j & 1, abort, p.timeout_ns)) { ok = false; break; }
-          tc_fence_after_sync();
-          issue_pv(1, slot_v, j > 0);
-          mma_commit(&bars->o_done[1]);
-        }
-        mma_commit(&bars->kv_empty[slot_v]);
-        if (next) {
-          if (j + 1 < n1) { issue_s(1, slot_k); mma_commit(&bars->s_full[1]); }
-          mma_commit(&bars->kv_empty[slot_k]);
-        }
-      }
-      if (!ok) raise_abort(abort, p.status);
-      // Every MMA must be complete before TMEM is released.
-      mma_commit(&bars->mma_drain);
-      volatile int never = 0;
-      wait_bar(&bars->mma_drain, 0, &never, p.timeout_ns);
     }
-  } else if (warp < 8) {
+  } else {
+    regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int sub = warp >> 2;
     const int n_tiles = sub == 0 ? n0 : n1;
@@ -324,11 +337,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (key0 + c * 32 + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
       }
 
-      float mx = -INFINITY;
+      // row max: eight independent 3-input max chains over the 128 scores, then a small tree
+#define FA2_S(f) __uint_as_float(s[(f) >> 5][(f) & 31])
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int k = 0; k < 8; ++k) mx8[k] = FA2_S(k);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+      for (int f = 8; f < 120; f += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], FA2_S(f + k), FA2_S(f + 8 + k));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], FA2_S(120 + k));
+#undef FA2_S
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const float m_cand = fmaxf(m, mx * sl2);
       const bool move = (j == 0) || (m_cand > m + kRescaleLog2);
       const float m_new = move ? m_cand : m;
@@ -336,20 +358,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = !move ? 1.f : (m == -INFINITY ? 0.f : ex2_approx(m - m_new));
       const float off = m_new == -INFINITY ? 0.f : m_new;
 
-      float rs = 0.f;
+      // P = 2^(s * scale*log2e - offset), packed pairwise; row sum in four packed accumulators
+      const float2 c2 = make_float2(sl2, sl2);
+      const float2 o2 = make_float2(-off, -off);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
       uint32_t pk[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][e]), sl2, -off));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][e + 1]), sl2, -off));
-          rs += p0 + p1;
-          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+          const float2 t = __ffma2_rn(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), c2, o2);
+          const float2 pe = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+          acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], pe);
+          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(pe.x, pe.y);
         }
+        // the first half of P goes to TMEM while the second half is computed
+        if (c == 1) tmem_st32(tS, pk[0]);
+      }
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      const float rs = a.x + a.y;
       l = l * alpha + rs;
       m = m_new;
-      tmem_st32(tS, pk[0]);
       tmem_st32(tS + 32, pk[1]);
 
       // correction of the running output when some row of this warp moved its offset
