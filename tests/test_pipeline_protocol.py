@@ -1,0 +1,307 @@
+"""Model check of the tensor-core kernel's barrier protocol (host-only).
+
+The forward kernel coordinates a TMA producer, one MMA-issuing thread and two
+softmax warpgroups through mbarriers.  This test restates that protocol in a
+small discrete-event model and runs it under many random interleavings
+(TMA copies finish in any order, MMAs finish in issue order, roles advance
+in random order).  It fails on:
+
+* an arrival on an mbarrier phase that has already received all of its
+  expected arrivals (undefined on the hardware);
+* a parity wait issued while the barrier is two or more phases past the
+  phase the waiter means (the parity would be ambiguous);
+* a TMA copy into a ring slot whose previous contents were not released;
+* an MMA reading a slot that does not hold the load it expects;
+* a deadlock.
+
+The model mirrors the producer, issuer and softmax loops of the kernel in
+exact_attention_17_gb300/csrc/fa2_fwd_sm103.cuh; a change to that protocol
+must be made here too.
+"""
+import random
+
+import pytest
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+class MBarrier:
+    def __init__(self, name, count):
+        self.name, self.count = name, count
+        self.completed = 0          # completed phases
+        self.pending = count        # arrivals still expected in the current phase
+        self.tx = 0                 # outstanding transaction bytes
+
+    def _maybe_complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.completed += 1
+            self.pending = self.count
+
+    def arrive(self, tx_bytes=0):
+        if self.pending == 0:
+            raise ProtocolError(f"{self.name}: arrival beyond the expected count")
+        self.pending -= 1
+        self.tx += tx_bytes
+        self._maybe_complete()
+
+    def complete_tx(self, nbytes):
+        self.tx -= nbytes
+        self._maybe_complete()
+
+    def done(self, phase):
+        """Has phase number `phase` completed?  Checks the parity hazard."""
+        if self.completed > phase + 1:
+            raise ProtocolError(f"{self.name}: waiter for phase {phase} sees {self.completed} "
+                                "completed phases (parity aliasing)")
+        return self.completed == phase + 1
+
+
+class Sim:
+    def __init__(self, stages, n0, n1, seed, rescale_prob=0.3):
+        self.rng = random.Random(seed)
+        self.S, self.NG = stages, stages // 2
+        self.n = (n0, n1)
+        self.nmax = max(n0, n1)
+        self.rescale_prob = rescale_prob
+        TILE = 1
+        self.TILE = TILE
+        self.q_full = MBarrier("q_full", 1)
+        self.slot_full = [MBarrier(f"slot_full[{i}]", 1) for i in range(stages)]
+        self.group_full = [MBarrier(f"group_full[{i}]", 1) for i in range(self.NG)]
+        self.slot_empty = [MBarrier(f"slot_empty[{i}]", 1) for i in range(stages)]
+        self.s_full = [MBarrier(f"s_full[{i}]", 1) for i in range(2)]
+        self.p_ready = [MBarrier(f"p_ready[{i}]", 1) for i in range(2)]
+        self.o_done = [MBarrier(f"o_done[{i}]", 1) for i in range(2)]
+        self.drain = MBarrier("mma_drain", 1)
+        self.slot = [None] * stages           # ("loading"|"ready"|"free", load id)
+        for i in range(stages):
+            self.slot[i] = ("free", None)
+        self.tma_inflight = []                # (barrier, slot or None, load id, bytes)
+        self.mma_queue = []                   # ops in issue order: ("mma", reads) | ("commit", bar)
+        self.released = set()
+
+    # -------------------------------------------------------- async engines
+    def tma_load(self, bar, slot, g):
+        if slot is not None:
+            state, _ = self.slot[slot]
+            if state != "free":
+                raise ProtocolError(f"TMA load {g} into slot {slot} still in use ({self.slot[slot]})")
+            self.slot[slot] = ("loading", g)
+        self.tma_inflight.append((bar, slot, g, self.TILE))
+
+    def finish_one_tma(self):
+        bar, slot, g, nb = self.tma_inflight.pop(self.rng.randrange(len(self.tma_inflight)))
+        if slot is not None:
+            self.slot[slot] = ("ready", g)
+        bar.complete_tx(nb)
+
+    def mma(self, reads):
+        for slot, g in reads:
+            if self.slot[slot] != ("ready", g):
+                raise ProtocolError(f"MMA expects load {g} in slot {slot}, finds {self.slot[slot]}")
+        self.mma_queue.append(("mma", reads))
+
+    def commit(self, bar, release=None):
+        self.mma_queue.append(("commit", bar, release))
+
+    def finish_one_mma(self):
+        op = self.mma_queue.pop(0)
+        if op[0] == "commit":
+            _, bar, release = op
+            if release is not None:
+                slot, g = release
+                if self.slot[slot] != ("ready", g):
+                    raise ProtocolError(f"release of load {g}: slot {slot} holds {self.slot[slot]}")
+                self.slot[slot] = ("free", None)
+            bar.arrive()
+
+    # -------------------------------------------------------- roles
+    def producer(self):
+        """One full barrier per ring slot; load g (K_j for g = 2j, V_j for
+        g = 2j + 1) waits for the release of load g - STAGES in its slot."""
+        S, nmax = self.S, self.nmax
+        self.q_full.arrive(tx_bytes=self.TILE)
+        self.tma_load(self.q_full, None, "Q")
+        for g in range(2 * nmax):
+            slot, r = g % S, g // S
+            if r > 0:
+                while not self.slot_empty[slot].done(r - 1):
+                    yield
+            self.slot_full[slot].arrive(tx_bytes=self.TILE)
+            self.tma_load(self.slot_full[slot], slot, g)
+            yield
+
+    def issuer(self):
+        S, NG, nmax = self.S, self.NG, self.nmax
+        n0, n1 = self.n
+
+        def issue_s(sub, g):
+            self.mma([(g % S, g)])
+            self.commit(self.s_full[sub])
+
+        def issue_pv(sub, g):
+            self.mma([(g % S, g)])
+            self.commit(self.o_done[sub])
+
+        while not self.q_full.done(0):
+            yield
+        while not self.slot_full[0].done(0):
+            yield
+        if n0 > 0:
+            issue_s(0, 0)
+        if n1 > 0:
+            issue_s(1, 0)
+        self.commit(self.slot_empty[0], release=(0, 0))
+        for j in range(nmax):
+            gv, gk = 2 * j + 1, 2 * j + 2
+            nxt = j + 1 < nmax
+            while not self.slot_full[gv % S].done(gv // S):
+                yield
+            if j < n0:
+                while not self.p_ready[0].done(j):
+                    yield
+                issue_pv(0, gv)
+            if nxt:
+                while not self.slot_full[gk % S].done(gk // S):
+                    yield
+                if j + 1 < n0:
+                    issue_s(0, gk)
+            if j < n1:
+                while not self.p_ready[1].done(j):
+                    yield
+                issue_pv(1, gv)
+            self.commit(self.slot_empty[gv % S], release=(gv % S, gv))
+            if nxt:
+                if j + 1 < n1:
+                    issue_s(1, gk)
+                self.commit(self.slot_empty[gk % S], release=(gk % S, gk))
+            yield
+        self.commit(self.drain)
+        while not self.drain.done(0):
+            yield
+
+    def softmax(self, sub):
+        n = self.n[sub]
+        for j in range(n):
+            while not self.s_full[sub].done(j):
+                yield
+            yield
+            if j > 0 and self.rng.random() < self.rescale_prob:
+                while not self.o_done[sub].done(j - 1):
+                    yield
+            self.p_ready[sub].arrive()
+        if n > 0:
+            while not self.o_done[sub].done(n - 1):
+                yield
+
+    # -------------------------------------------------------- scheduler
+    def run(self):
+        roles = {"producer": self.producer(), "issuer": self.issuer(),
+                 "softmax0": self.softmax(0), "softmax1": self.softmax(1)}
+        steps = 0
+        while roles or self.tma_inflight or self.mma_queue:
+            steps += 1
+            if steps > 200000:
+                raise ProtocolError("no progress (deadlock)")
+            choices = list(roles) + (["tma"] if self.tma_inflight else []) + \
+                (["mma"] if self.mma_queue else [])
+            c = self.rng.choice(choices)
+            if c == "tma":
+                self.finish_one_tma()
+            elif c == "mma":
+                self.finish_one_mma()
+            else:
+                try:
+                    next(roles[c])
+                except StopIteration:
+                    del roles[c]
+        # every load released exactly once, nothing left in flight
+        for i, st in enumerate(self.slot):
+            if st[0] == "loading":
+                raise ProtocolError(f"slot {i} still loading at exit")
+
+
+CASES = []
+for stages in (4, 8):
+    for nmax in list(range(1, 11)) + [17]:
+        CASES.append((stages, nmax, nmax))          # non-causal: both sub-tiles, same range
+        CASES.append((stages, nmax - 1, nmax) if nmax > 1 else (stages, 1, 1))  # causal pair
+        CASES.append((stages, nmax, 0))             # second sub-tile past the end
+
+
+@pytest.mark.parametrize("stages,n0,n1", CASES)
+def test_protocol_random_interleavings(stages, n0, n1):
+    for seed in range(40):
+        Sim(stages, n0, n1, seed).run()
+
+
+def test_model_catches_early_rearm():
+    """A grouped variant of the protocol (V_(t-1) and K_t landing on one
+    barrier, STAGES/2 barriers reused in turn) whose producer only waited for
+    its own slots re-armed a barrier before its previous phase had been
+    consumed when the last group held only V.  That ordering faulted the GPU;
+    the model must reject it."""
+
+    class GroupedSim(Sim):
+        def producer(self):
+            S, NG, nmax = self.S, self.NG, self.nmax
+            self.q_full.arrive(tx_bytes=self.TILE)
+            self.tma_load(self.q_full, None, "Q")
+            for t in range(nmax + 1):
+                g_first = 0 if t == 0 else 2 * t - 1
+                g_last = 2 * t if t < nmax else 2 * t - 1
+                for g in range(g_first, g_last + 1):
+                    r = g // S
+                    if r > 0:
+                        while not self.slot_empty[g % S].done(r - 1):
+                            yield
+                full = self.group_full[t % NG]
+                full.arrive(tx_bytes=(g_last - g_first + 1) * self.TILE)
+                for g in range(g_first, g_last + 1):
+                    self.tma_load(full, g % S, g)
+                yield
+
+        def issuer(self):
+            S, NG, nmax = self.S, self.NG, self.nmax
+            n0, n1 = self.n
+            while not self.q_full.done(0):
+                yield
+            while not self.group_full[0].done(0):
+                yield
+            for sub in (0, 1):
+                if self.n[sub] > 0:
+                    self.mma([(0, 0)])
+                    self.commit(self.s_full[sub])
+            self.commit(self.slot_empty[0], release=(0, 0))
+            for j in range(nmax):
+                t = j + 1
+                gv, gk = 2 * j + 1, 2 * j + 2
+                nxt = j + 1 < nmax
+                while not self.group_full[t % NG].done(t // NG):
+                    yield
+                for sub in (0, 1):
+                    if j < self.n[sub]:
+                        while not self.p_ready[sub].done(j):
+                            yield
+                        self.mma([(gv % S, gv)])
+                        self.commit(self.o_done[sub])
+                    if nxt and j + 1 < self.n[sub]:
+                        self.mma([(gk % S, gk)])
+                        self.commit(self.s_full[sub])
+                self.commit(self.slot_empty[gv % S], release=(gv % S, gv))
+                if nxt:
+                    self.commit(self.slot_empty[gk % S], release=(gk % S, gk))
+                yield
+            self.commit(self.drain)
+            while not self.drain.done(0):
+                yield
+
+    failures = 0
+    for seed in range(200):
+        try:
+            GroupedSim(4, 1, 2, seed).run()
+        except ProtocolError:
+            failures += 1
+    assert failures > 0
