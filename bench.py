@@ -148,6 +148,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- multi-rank aggregation
+
+def job_time_ms(local_ms: float, dist=None, device=None) -> float:
+    """Elapsed time of the whole job: the slowest replica's timed region."""
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step: float, steps: int, world: int, job_ms: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of the workload."""
+    return flops_per_step * steps * world / (job_ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- oracle (CPU) timing
 
 def oracle_sample_rate(w, Q, K, V, budget_s: float, seed: int = 0):
@@ -316,10 +331,7 @@ def main():
     kernel_ms = sum(launch_ms)
     total_ms = t_begin.elapsed_time(t_end)
     timed_ms = kernel_ms if flush is not None else total_ms
-    t = torch.tensor([timed_ms], device=dev, dtype=torch.float64)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    job_ms = float(t.item())
+    job_ms = job_time_ms(timed_ms, dist, dev)
 
     # end to end through the public call: pinned host inputs -> device -> forward -> host result
     Qp, Kp, Vp = Qh.pin_memory(), Kh.pin_memory(), Vh.pin_memory()
@@ -346,10 +358,7 @@ def main():
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-    te = torch.tensor([e0.elapsed_time(e1)], device=dev, dtype=torch.float64)
-    if dist:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te.item())
+    e2e_ms = job_time_ms(e0.elapsed_time(e1), dist, dev)
     h2d = (Qp.numel() + Kp.numel() + Vp.numel()) * 2
     d2h = (Op.numel() + Lp.numel()) * 4
 
@@ -362,7 +371,7 @@ def main():
     mean_launch_ms = statistics.mean(launch_ms)
     achieved = w.flops / (mean_launch_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
-    value = w.flops * args.steps * world / (job_ms * 1e-3) / 1e12
+    value = job_tflops(w.flops, args.steps, world, job_ms)
     traffic = recorded_traffic(w.name)
 
     cpu = None
@@ -403,7 +412,7 @@ def main():
             "mean_launch_ms": round(mean_launch_ms, 4),
         },
         "cpu_baseline": cpu,
-        "e2e": {"value": round(w.flops * args.e2e_steps * world / (e2e_ms * 1e-3) / 1e12, 2),
+        "e2e": {"value": round(job_tflops(w.flops, args.e2e_steps, world, e2e_ms), 2),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
         "clocks": clk,
