@@ -249,6 +249,8 @@ def main():
                     help="seconds of oracle work for the cpu_baseline field (0 = skip)")
     ap.add_argument("--reference-step-s", type=float, default=None,
                     help="oracle seconds per reference step (default: ~120 s over all steps)")
+    ap.add_argument("--num-splits", type=int, default=1,
+                    help="split the keys into this many ranges (split-KV forward + merge)")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count (smaller profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -293,8 +295,14 @@ def main():
     else:
         l2_note = f"inputs {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"
 
+    workspace = None
+    if args.num_splits > 1:
+        need = fa2.fa2_splitkv_workspace_bytes(w.B, w.H, w.Nq, w.d, args.num_splits)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+
     def step(s):
-        fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, out=O, lse=L, stream=s)
+        fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, out=O, lse=L, stream=s,
+                    num_splits=args.num_splits, workspace=workspace)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -342,7 +350,8 @@ def main():
         Q.copy_(Qp, non_blocking=True)
         K.copy_(Kp, non_blocking=True)
         V.copy_(Vp, non_blocking=True)
-        fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, out=O, lse=L, stream=stream)
+        fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, out=O, lse=L, stream=stream,
+                    num_splits=args.num_splits, workspace=workspace)
         Op.copy_(O, non_blocking=True)
         Lp.copy_(L, non_blocking=True)
 
@@ -395,7 +404,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": workload_config(w, l2_note),
+        "config": dict(workload_config(w, l2_note), num_splits=args.num_splits),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": {
             "bound": "tensor",
@@ -414,7 +423,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_tflops(w.flops, args.e2e_steps, world, e2e_ms), 2),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if args.num_splits > 1 else 1),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

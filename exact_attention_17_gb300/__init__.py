@@ -27,9 +27,13 @@ FA2_ERR_DEVICE = 9
 # Every function the C header declares, with its ctypes signature.
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _FORWARD_ARGS = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]
+_Z, _LL = ctypes.c_size_t, ctypes.c_longlong
 SIGNATURES = {
     "fa2_forward": (_I, _FORWARD_ARGS),
     "fa2_forward_simt": (_I, _FORWARD_ARGS),
+    "fa2_splitkv_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
+    "fa2_forward_splitkv": (_I, _FORWARD_ARGS[:-1] + [_I, _P, _Z, _P]),
+    "fa2_merge": (_I, [_P, _P, _I, _LL, _I, _P, _P, _P]),
     "fa2_status_string": (ctypes.c_char_p, [_I]),
     "fa2_device_status": (_I, [_P, _I]),
 }
@@ -69,6 +73,22 @@ def fa2_forward_simt(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, stream) ->
                                       stream)
 
 
+def fa2_splitkv_workspace_bytes(B, H, Nq, d, num_splits) -> int:
+    return library().fa2_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+
+
+def fa2_forward_splitkv(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, num_splits, workspace,
+                        workspace_size, stream) -> int:
+    """Raw C call of the split-KV forward (caller-provided device workspace)."""
+    return library().fa2_forward_splitkv(Q, K, V, O, LSE, B, H, Nq, Nk, d, int(bool(causal)), scale,
+                                         num_splits, workspace, workspace_size, stream)
+
+
+def fa2_merge(O_parts, LSE_parts, num_parts, rows, d, O, LSE, stream) -> int:
+    """Raw C call of the merge of partial attention results."""
+    return library().fa2_merge(O_parts, LSE_parts, num_parts, rows, d, O, LSE, stream)
+
+
 def fa2_status_string(status: int) -> str:
     return library().fa2_status_string(status).decode()
 
@@ -86,13 +106,15 @@ def _stream_handle(stream):
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-            stream=None, impl: str = "tc"):
+            stream=None, impl: str = "tc", num_splits: int = 1, workspace=None):
     """Attention forward on torch CUDA tensors.
 
     q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; all contiguous on one device.
     Returns (O fp32 [B,H,Nq,d], LSE fp32 [B,H,Nq]).  ``scale`` defaults to
     1/sqrt(d) rounded to float32.  ``impl="simt"`` runs the CUDA-core
     cross-check implementation instead of the tensor-core one.
+    ``num_splits > 1`` runs the split-KV forward over that many key ranges;
+    its workspace (a uint8 CUDA tensor) is allocated here unless given.
     """
     import torch
 
@@ -112,10 +134,50 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     for name, t, shape in (("out", out, (B, H, Nq, d)), ("lse", lse, (B, H, Nq))):
         if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
             raise ValueError(f"{name} must be a contiguous fp32 tensor of shape {shape} on {q.device}")
-    fn = {"tc": fa2_forward, "simt": fa2_forward_simt}[impl]
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            B, H, Nq, Nk, d, causal, float(scale))
     with torch.cuda.device(q.device):
-        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                B, H, Nq, Nk, d, causal, float(scale), _stream_handle(stream))
+        if num_splits > 1:
+            if impl != "tc":
+                raise ValueError("split-KV runs on the tensor-core path only")
+            need = fa2_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+            if workspace is None:
+                workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+            rc = fa2_forward_splitkv(*args, num_splits, workspace.data_ptr(), workspace.numel(),
+                                     _stream_handle(stream))
+            name = "fa2_forward_splitkv"
+        else:
+            fn = {"tc": fa2_forward, "simt": fa2_forward_simt}[impl]
+            rc = fn(*args, _stream_handle(stream))
+            name = "fa2_forward" if impl == "tc" else "fa2_forward_simt"
     if rc != FA2_OK:
-        raise FA2Error(rc, "fa2_forward" if impl == "tc" else "fa2_forward_simt")
+        raise FA2Error(rc, name)
+    return out, lse
+
+
+def merge(o_parts, lse_parts, out=None, lse=None, stream=None):
+    """Merge partial results over disjoint key subsets (fa2_merge).
+
+    o_parts fp32 [P, ..., d], lse_parts fp32 [P, ...] (contiguous CUDA
+    tensors); returns (O [..., d], LSE [...]).
+    """
+    import torch
+
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise ValueError("parts must be fp32")
+    if not (o_parts.is_cuda and lse_parts.is_contiguous() and o_parts.is_contiguous()):
+        raise ValueError("parts must be contiguous CUDA tensors")
+    P, d = o_parts.shape[0], o_parts.shape[-1]
+    if tuple(lse_parts.shape) != tuple(o_parts.shape[:-1]):
+        raise ValueError("lse_parts must match o_parts without the last dimension")
+    rows = lse_parts.numel() // P if P else 0
+    if out is None:
+        out = torch.empty(o_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    with torch.cuda.device(o_parts.device):
+        rc = fa2_merge(o_parts.data_ptr(), lse_parts.data_ptr(), P, rows, d, out.data_ptr(),
+                       lse.data_ptr(), _stream_handle(stream))
+    if rc != FA2_OK:
+        raise FA2Error(rc, "fa2_merge")
     return out, lse

@@ -18,6 +18,7 @@ namespace {
 __device__ int g_device_status = 0;
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per barrier wait
+constexpr int kMaxSplits = 64;
 constexpr int kMaxDevices = 64;
 
 struct DriverFns {
@@ -137,16 +138,14 @@ int validate(const void* Q, const void* K, const void* V, const float* O, const 
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-}  // namespace
-
-extern "C" int fa2_forward(const void* Q, const void* K, const void* V, float* O, float* LSE, int B,
-                           int H, int Nq, int Nk, int d, int causal, float scale,
-                           fa2_stream_t stream) {
-  Problem pr;
-  int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr);
-  if (rc != FA2_OK || pr.empty) return rc;
+// Launch of the tensor-core kernel over `splits` key ranges of `tiles_per_split`
+// tiles each (splits == 1: the whole key range, outputs O and LSE directly).
+int launch_forward(const void* Q, const void* K, const void* V, float* O, float* LSE,
+                   const Problem& pr, int causal, float scale, int splits, int tiles_per_split,
+                   float* O_part, float* LSE_part, cudaStream_t s) {
+  const int Nq = pr.Nq, Nk = pr.Nk, d = pr.d;
   const long long pairs = (static_cast<long long>(Nq) + 255) / 256;
-  if (pairs * pr.BH > 0x7fffffffLL) return FA2_ERR_SHAPE;
+  if (pairs * pr.BH * splits > 0x7fffffffLL) return FA2_ERR_SHAPE;
 
   CUtensorMap mq, mk, mv;
   if (!encode_map(&mq, Q, d, Nq, static_cast<int>(pr.BH)) ||
@@ -163,14 +162,104 @@ extern "C" int fa2_forward(const void* Q, const void* K, const void* V, float* O
   p.q_pairs = static_cast<int>(pairs);
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = kWaitTimeoutNs;
+  p.num_splits = splits;
+  p.tiles_per_split = tiles_per_split;
+  p.O_part = O_part;
+  p.LSE_part = LSE_part;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
     return FA2_ERR_LAUNCH;
 
-  const unsigned grid = static_cast<unsigned>(pairs * pr.BH);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned grid = static_cast<unsigned>(pairs * pr.BH * splits);
   const cudaError_t e = d == 64 ? fa2host::launch_tc_d64(causal != 0, mq, mk, mv, p, grid, s)
                                 : fa2host::launch_tc_d128(causal != 0, mq, mk, mv, p, grid, s);
   return e == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
+}
+
+int key_tiles(int Nk) { return (Nk + 127) / 128; }
+
+// Key ranges actually used for a requested split count: ranges of
+// ceil(tiles / requested) tiles, as many as that takes.
+void split_plan(int Nk, int requested, int* splits, int* tiles_per_split) {
+  const int tiles = key_tiles(Nk);
+  const int want = requested < 1 ? 1 : (requested > tiles ? tiles : requested);
+  *tiles_per_split = (tiles + want - 1) / want;
+  *splits = (tiles + *tiles_per_split - 1) / *tiles_per_split;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace layout for `splits` ranges: O_part, then LSE_part (256-byte aligned).
+size_t workspace_bytes(long long BH, int Nq, int d, int splits) {
+  const size_t rows = static_cast<size_t>(BH) * Nq;
+  return align256(static_cast<size_t>(splits) * rows * d * 4) + align256(static_cast<size_t>(splits) * rows * 4);
+}
+
+}  // namespace
+
+extern "C" int fa2_forward(const void* Q, const void* K, const void* V, float* O, float* LSE, int B,
+                           int H, int Nq, int Nk, int d, int causal, float scale,
+                           fa2_stream_t stream) {
+  Problem pr;
+  int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr);
+  if (rc != FA2_OK || pr.empty) return rc;
+  return launch_forward(Q, K, V, O, LSE, pr, causal, scale, 1, key_tiles(Nk), nullptr, nullptr,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t fa2_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 0 || H < 0 || Nq < 0 || num_splits < 1 || (d != 64 && d != 128)) return 0;
+  return workspace_bytes(static_cast<long long>(B) * H, Nq, d, num_splits);
+}
+
+extern "C" int fa2_forward_splitkv(const void* Q, const void* K, const void* V, float* O, float* LSE,
+                                   int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                   int num_splits, void* workspace, size_t workspace_size,
+                                   fa2_stream_t stream) {
+  Problem pr;
+  int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr);
+  if (rc != FA2_OK || pr.empty) return rc;
+  if (num_splits < 1 || num_splits > kMaxSplits) return FA2_ERR_SHAPE;
+  int splits = 1, tps = 1;
+  split_plan(Nk, num_splits, &splits, &tps);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (splits == 1)
+    return launch_forward(Q, K, V, O, LSE, pr, causal, scale, 1, tps, nullptr, nullptr, s);
+  const size_t need = workspace_bytes(pr.BH, Nq, d, splits);
+  if (!workspace) return FA2_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA2_ERR_ALIGN;
+  if (workspace_size < need || !device_range_ok(workspace, need)) return FA2_ERR_MEMORY;
+  const size_t rows = static_cast<size_t>(pr.BH) * Nq;
+  float* O_part = static_cast<float*>(workspace);
+  float* LSE_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             align256(static_cast<size_t>(splits) * rows * d * 4));
+  rc = launch_forward(Q, K, V, O, LSE, pr, causal, scale, splits, tps, O_part, LSE_part, s);
+  if (rc != FA2_OK) return rc;
+  return fa2host::launch_combine(d, O_part, LSE_part, splits, static_cast<long long>(rows), O, LSE, s) ==
+                 cudaSuccess
+             ? FA2_OK
+             : FA2_ERR_LAUNCH;
+}
+
+extern "C" int fa2_merge(const float* O_parts, const float* LSE_parts, int num_parts, long long rows,
+                         int d, float* O, float* LSE, fa2_stream_t stream) {
+  if (rows < 0 || num_parts < 0) return FA2_ERR_SHAPE;
+  if (rows == 0) return FA2_OK;
+  if (num_parts < 1 || num_parts > kMaxSplits) return FA2_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA2_ERR_HEADDIM;
+  if (!O_parts || !LSE_parts || !O || !LSE) return FA2_ERR_NULL;
+  if (((reinterpret_cast<uintptr_t>(O_parts) | reinterpret_cast<uintptr_t>(O)) & 15u) != 0 ||
+      ((reinterpret_cast<uintptr_t>(LSE_parts) | reinterpret_cast<uintptr_t>(LSE)) & 3u) != 0)
+    return FA2_ERR_ALIGN;
+  int rc = device_ready();
+  if (rc != FA2_OK) return rc;
+  const size_t r = static_cast<size_t>(rows);
+  if (!device_range_ok(O_parts, r * num_parts * d * 4) || !device_range_ok(LSE_parts, r * num_parts * 4) ||
+      !device_range_ok(O, r * d * 4) || !device_range_ok(LSE, r * 4))
+    return FA2_ERR_MEMORY;
+  return fa2host::launch_combine(d, O_parts, LSE_parts, num_parts, rows, O, LSE,
+                                 reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA2_OK
+             : FA2_ERR_LAUNCH;
 }
 
 extern "C" int fa2_forward_simt(const void* Q, const void* K, const void* V, float* O, float* LSE,

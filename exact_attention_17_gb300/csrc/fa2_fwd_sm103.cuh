@@ -54,8 +54,8 @@ namespace fa2dev {
 constexpr int kDevErrTimeout = 1;
 
 struct FwdParams {
-  float* O;        // [BH, Nq, D] fp32
-  float* LSE;      // [BH, Nq]    fp32
+  float* O;        // [BH, Nq, D] fp32 (num_splits == 1)
+  float* LSE;      // [BH, Nq]    fp32 (num_splits == 1)
   int Nq;
   int Nk;
   int BH;
@@ -63,6 +63,16 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   int* status;     // device status word
   unsigned long long timeout_ns;
+  // Split of the keys into ranges processed by separate CTAs ("FlashDecoding",
+  // "Flash Attention 全解析(上)" section 4): range s covers key tiles
+  // [s * tiles_per_split, (s + 1) * tiles_per_split).  With num_splits > 1
+  // each CTA writes its range's normalised output and logsumexp to
+  // O_part [num_splits, BH, Nq, D] and LSE_part [num_splits, BH, Nq]; a row
+  // with no kept key in the range gets O = 0 and LSE = -inf.
+  int num_splits;
+  int tiles_per_split;
+  float* O_part;
+  float* LSE_part;
 };
 
 constexpr int kRowsPerSub = 128;   // tcgen05 M
@@ -107,15 +117,18 @@ __device__ __forceinline__ void raise_abort(volatile int* abort, int* status) {
   atomicOr(status, kDevErrTimeout);
 }
 
-// Number of K/V tiles query sub-tile `sub` of pair `u` visits (0 = no rows).
+// Number of K/V tiles query sub-tile `sub` of pair `u` visits within the key
+// tile range [t_begin, t_end) (0 = no rows, or every key masked).
 template <bool CAUSAL>
-__device__ __forceinline__ int kv_tiles_for(int u, int sub, int Nq, int Nk) {
+__device__ __forceinline__ int kv_tiles_for(int u, int sub, int Nq, int t_begin, int t_end) {
   const int first = u * 2 * kRowsPerSub + sub * kRowsPerSub;
   if (first >= Nq) return 0;
-  const int all = (Nk + kKeysPerTile - 1) / kKeysPerTile;
-  if (!CAUSAL) return all;
-  const int last = min(first + kRowsPerSub - 1, Nq - 1);
-  return min(all, last / kKeysPerTile + 1);
+  int stop = t_end;
+  if (CAUSAL) {
+    const int last = min(first + kRowsPerSub - 1, Nq - 1);
+    stop = min(stop, last / kKeysPerTile + 1);
+  }
+  return max(0, stop - t_begin);
 }
 
 template <int D, bool CAUSAL>
@@ -140,15 +153,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: (pair u of query sub-tiles, b*H + h).  Pairs of one head are
-  // adjacent so that concurrently running CTAs share K/V tiles through L2;
-  // under the causal mask the heaviest pairs of a head start first.
+  // Work item: (pair u of query sub-tiles, key range, b*H + h).  Pairs of one
+  // head and range are adjacent so that concurrently running CTAs share K/V
+  // tiles through L2; under the causal mask the heaviest pairs start first.
   const int U = p.q_pairs;
-  const int bh = blockIdx.x / U;
-  int u = blockIdx.x - bh * U;
+  const int item = blockIdx.x / U;
+  const int bh = item / p.num_splits;
+  const int split = item - bh * p.num_splits;
+  int u = blockIdx.x - item * U;
   if (CAUSAL) u = U - 1 - u;
-  const int n0 = kv_tiles_for<CAUSAL>(u, 0, p.Nq, p.Nk);
-  const int n1 = kv_tiles_for<CAUSAL>(u, 1, p.Nq, p.Nk);
+  const int all_tiles = (p.Nk + kKeysPerTile - 1) / kKeysPerTile;
+  const int t_begin = split * p.tiles_per_split;
+  const int t_end = min(all_tiles, t_begin + p.tiles_per_split);
+  const int n0 = kv_tiles_for<CAUSAL>(u, 0, p.Nq, t_begin, t_end);
+  const int n1 = kv_tiles_for<CAUSAL>(u, 1, p.Nq, t_begin, t_end);
   const int nmax = max(n0, n1);
   const int q_row0 = u * 2 * kRowsPerSub;
 
@@ -209,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
             for (int c = 0; c < NCH; ++c)
               tma_load_3d(sKV + slot * TILE + c * kChunkBytes, map, &bars->kv_full[slot], c * 64,
-                          j * kKeysPerTile, bh);
+                          (t_begin + j) * kKeysPerTile, bh);
             ++issued;
           }
         }
@@ -325,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
 
       // masks: keys past the end, and keys after the query under the causal mask
-      const int key0 = j * kKeysPerTile;
+      const int key0 = (t_begin + j) * kKeysPerTile;
       const bool tail = key0 + kKeysPerTile > p.Nk;
       const bool diag = CAUSAL && key0 + kKeysPerTile - 1 > sub_row0;
       if (tail || diag) {
@@ -408,15 +426,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
     }
 
+    // Outputs of this row: the final ones, or this key range's partial ones.
+    const bool store = qi < p.Nq;
+    const size_t row_id = (static_cast<size_t>(p.num_splits > 1 ? split : 0) * p.BH + bh) * p.Nq + qi;
+    float* orow = (p.num_splits > 1 ? p.O_part : p.O) + row_id * D;
+    float* lse_out = (p.num_splits > 1 ? p.LSE_part : p.LSE) + row_id;
+    if (n_tiles == 0 && store && p.num_splits > 1) {
+      // no kept key in this range: contributes nothing to the merge
+      for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *lse_out = -INFINITY;
+    }
     if (n_tiles > 0 && ok) {
       if (!__all_sync(0xffffffffu,
                       wait_bar(&bars->o_done[sub], (n_tiles - 1) & 1, abort, p.timeout_ns))) {
         ok = false;
       } else {
         tc_fence_after_sync();
-        const float inv_l = 1.f / l;
-        const bool store = qi < p.Nq;
-        float* orow = p.O + (static_cast<size_t>(bh) * p.Nq + qi) * D;
+        // l == 0 only for a row whose every key in this range is masked
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -431,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (store) p.LSE[static_cast<size_t>(bh) * p.Nq + qi] = (m + __log2f(l)) * 0.69314718055994531f;
+        if (store) *lse_out = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
     if (!ok) raise_abort(abort, p.status);

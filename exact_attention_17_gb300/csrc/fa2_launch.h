@@ -23,4 +23,8 @@ cudaError_t launch_tc_d128(bool causal, const CUtensorMap& mq, const CUtensorMap
                            cudaStream_t s);
 cudaError_t launch_simt(int d, bool causal, const fa2dev::SimtParams& p, dim3 grid, cudaStream_t s);
 
+// Merge of S partial results (normalised O [S, R, d], LSE [S, R]) into O [R, d], LSE [R].
+cudaError_t launch_combine(int d, const float* O_part, const float* LSE_part, int S, long long R,
+                           float* O, float* LSE, cudaStream_t s);
+
 }  // namespace fa2host

@@ -39,6 +39,8 @@
 #ifndef FA2_H
 #define FA2_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -82,6 +84,51 @@ int fa2_forward(const void *Q, const void *K, const void *V, float *O, float *LS
  */
 int fa2_forward_simt(const void *Q, const void *K, const void *V, float *O, float *LSE, int B,
                      int H, int Nq, int Nk, int d, int causal, float scale, fa2_stream_t stream);
+
+/*
+ * Bytes of device workspace fa2_forward_splitkv needs for `num_splits` key
+ * ranges: num_splits * B*H*Nq * (d + 1) * 4 bytes, rounded up.  0 for
+ * invalid arguments.  Pure host arithmetic (no CUDA call).
+ */
+size_t fa2_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
+
+/*
+ * Split-KV forward ("Flash Decoding", "Flash Attention 全解析(上)" section 4):
+ * the keys are cut into up to `num_splits` ranges of whole 128-key tiles
+ * (ceil(tiles / num_splits) tiles each) and every (b, h, Q block, range) is
+ * a separate thread block, so short-query / long-key problems fill the GPU.
+ * Each range's normalised output and logsumexp go to `workspace`; a second
+ * kernel merges them into O and LSE (the merge of fa2_merge).  Same
+ * arguments, results (up to rounding) and errors as fa2_forward, plus:
+ *   num_splits      1..64 (1, or a problem with a single key tile, runs
+ *                   fa2_forward and does not touch the workspace)
+ *   workspace       device memory, 256-byte aligned, caller-owned, at least
+ *                   fa2_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+ *                   bytes (FA2_ERR_NULL / FA2_ERR_ALIGN / FA2_ERR_MEMORY);
+ *                   its contents on return are unspecified
+ *   workspace_size  size of that buffer in bytes
+ */
+int fa2_forward_splitkv(const void *Q, const void *K, const void *V, float *O, float *LSE, int B,
+                        int H, int Nq, int Nk, int d, int causal, float scale, int num_splits,
+                        void *workspace, size_t workspace_size, fa2_stream_t stream);
+
+/*
+ * Merge of attention results computed over disjoint key subsets: the
+ * ring-attention merge of "FlashAttention 怎么做?online softmax 怎么更新?"
+ * (two parts) and the reduction step of Flash Decoding (many parts).  Part p
+ * holds, per row r, the normalised output O_parts[p][r][:] and the
+ * logsumexp LSE_parts[p][r] (natural log) over its keys; the result is
+ *     LSE[r] = log sum_p exp(LSE_parts[p][r])
+ *     O[r]   = sum_p exp(LSE_parts[p][r] - LSE[r]) O_parts[p][r]
+ * A part with LSE = -inf contributes nothing; if every part has -inf the row
+ * gets O = 0 and LSE = -inf.
+ *   O_parts    device fp32 [num_parts, rows, d], 16-byte aligned
+ *   LSE_parts  device fp32 [num_parts, rows], 4-byte aligned
+ *   num_parts  1..64;  rows >= 0 (0: nothing launched);  d: 64 or 128
+ *   O, LSE     device fp32 [rows, d] and [rows] outputs (must not overlap the parts)
+ */
+int fa2_merge(const float *O_parts, const float *LSE_parts, int num_parts, long long rows, int d,
+              float *O, float *LSE, fa2_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char *fa2_status_string(int status);

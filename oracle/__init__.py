@@ -2,11 +2,13 @@
 
 TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may import this package; the product library
-never does, and it shares no code with the CUDA path.  The arithmetic lives
-in ``attn_ref.c`` (plain three-pass softmax attention in double precision,
-"Flash Attention 全解析(上)" section 1.2, with the per-row logsumexp of
-"FlashAttention 怎么做?online softmax 怎么更新?", FlashAttention-2 follow-up);
-this module only compiles it with gcc and marshals numpy arrays through ctypes.
+never does, and it shares no code with the CUDA path.  The attention
+arithmetic lives in ``attn_ref.c`` (plain three-pass softmax attention in
+double precision, "Flash Attention 全解析(上)" section 1.2, with the per-row
+logsumexp of "FlashAttention 怎么做?online softmax 怎么更新?",
+FlashAttention-2 follow-up); this module compiles it with gcc and marshals
+numpy arrays through ctypes.  ``merge`` (the same page's ring-attention
+merge of partial results) is written here in numpy float64.
 
 Parity pins (checked by the CPU test suite): the pages' worked online-softmax
 example, an independent library routine (torch's float64 CPU attention) on
@@ -142,3 +144,27 @@ def attention(Q, K, V, causal: bool, scale: float, nthreads: int | None = None):
 def attention_rows(Q, K, V, causal: bool, scale: float, rows, nthreads: int | None = None):
     """Exact attention of selected rows (see ``Oracle.attention_rows``)."""
     return _default().attention_rows(Q, K, V, causal, scale, rows, nthreads)
+
+
+def merge(O_parts, LSE_parts):
+    """Merge of results over disjoint key subsets, in float64.
+
+    "FlashAttention 怎么做?online softmax 怎么更新?" (ring-attention question):
+    L = log(e^L1 + e^L2), O = e^(L1-L) O1 + e^(L2-L) O2, applied here to any
+    number of parts: L = log sum_p e^(L_p), O = sum_p e^(L_p - L) O_p.  A part
+    with L_p = -inf has no kept key and contributes nothing; a row whose
+    parts are all -inf gets O = 0, L = -inf.
+
+    O_parts [P, ..., d], LSE_parts [P, ...] -> (O [..., d], LSE [...]).
+    """
+    O_parts = np.asarray(O_parts, dtype=np.float64)
+    L = np.asarray(LSE_parts, dtype=np.float64)
+    m = np.max(L, axis=0)
+    finite = np.isfinite(m)
+    m_safe = np.where(finite, m, 0.0)
+    w = np.where(np.isfinite(L), np.exp(L - m_safe[None]), 0.0)
+    s = np.sum(w, axis=0)
+    lse = np.where(finite, m_safe + np.log(np.where(finite, s, 1.0)), -np.inf)
+    coef = np.where(finite[None], w / np.where(finite, s, 1.0)[None], 0.0)
+    O = np.sum(coef[..., None] * O_parts, axis=0)
+    return O, lse

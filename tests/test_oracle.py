@@ -387,3 +387,44 @@ def test_pins_pass_on_unmodified_copy(oracle_mod, tmp_path):
     lib = oracle_mod.compile_source(str(tmp_path / "copy.c"), str(tmp_path / "copy.so"))
     ok, failed = all_pins(oracle_mod.Oracle(lib))
     assert ok, failed
+
+
+# ---------------------------------------------------------------- merge of partial results
+
+def test_merge_of_key_partitions_equals_full(oracle_mod):
+    """Merging the oracle's results over a partition of the keys (any number
+    of parts, uneven, one part empty under the causal mask) gives the oracle's
+    result over all keys."""
+    rng = np.random.default_rng(12)
+    B, H, Nq, Nk, d = 1, 2, 30, 70, 16
+    Q, K, V = rand_bits(rng, (B, H, Nq, d), 2.0), rand_bits(rng, (B, H, Nk, d), 2.0), rand_bits(rng, (B, H, Nk, d))
+    cuts = [0, 7, 31, 32, 58, 70]
+    O, L = oracle_mod.attention(Q, K, V, False, 0.3)
+    parts = [oracle_mod.attention(Q, np.ascontiguousarray(K[:, :, a:b]), np.ascontiguousarray(V[:, :, a:b]), False, 0.3)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    Om, Lm = oracle_mod.merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    assert np.allclose(Om, O, atol=1e-12, rtol=0) and np.allclose(Lm, L, atol=1e-12, rtol=0)
+
+
+def test_merge_closed_forms(oracle_mod):
+    rng = np.random.default_rng(13)
+    O1 = rng.standard_normal((5, 8))
+    L1 = rng.standard_normal(5)
+    # one part: identity
+    O, L = oracle_mod.merge(O1[None], L1[None])
+    assert np.allclose(O, O1) and np.allclose(L, L1)
+    # two equal parts: same O, LSE + log 2
+    O, L = oracle_mod.merge(np.stack([O1, O1]), np.stack([L1, L1]))
+    assert np.allclose(O, O1, atol=1e-15) and np.allclose(L, L1 + math.log(2), atol=1e-15)
+    # an empty part (-inf) contributes nothing; all parts empty -> O = 0, LSE = -inf
+    Linf = np.full(5, -np.inf)
+    O, L = oracle_mod.merge(np.stack([O1, rng.standard_normal((5, 8))]), np.stack([L1, Linf]))
+    assert np.allclose(O, O1) and np.allclose(L, L1)
+    O, L = oracle_mod.merge(np.stack([O1, O1]), np.stack([Linf, Linf]))
+    assert np.all(O == 0) and np.all(np.isneginf(L))
+    # weights follow the pages' two-part formula e^(L1-L), e^(L2-L)
+    O2, L2 = rng.standard_normal((5, 8)), rng.standard_normal(5)
+    O, L = oracle_mod.merge(np.stack([O1, O2]), np.stack([L1, L2]))
+    Lr = np.log(np.exp(L1) + np.exp(L2))
+    assert np.allclose(L, Lr, atol=1e-14)
+    assert np.allclose(O, np.exp(L1 - Lr)[:, None] * O1 + np.exp(L2 - Lr)[:, None] * O2, atol=1e-14)
