@@ -23,6 +23,7 @@ FA2_ERR_TIMEOUT = 6
 FA2_ERR_SCALE = 7
 FA2_ERR_MEMORY = 8
 FA2_ERR_DEVICE = 9
+FA2_ERR_SCRATCH = 10
 
 # Every function the C header declares, with its ctypes signature.
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -34,6 +35,7 @@ SIGNATURES = {
     "fa2_splitkv_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "fa2_forward_splitkv": (_I, _FORWARD_ARGS[:-1] + [_I, _P, _Z, _P]),
     "fa2_merge": (_I, [_P, _P, _I, _LL, _I, _P, _P, _P]),
+    "fa2_forward_splitkv_static": (_I, _FORWARD_ARGS[:-1] + [_I, _P]),
     "fa2_status_string": (ctypes.c_char_p, [_I]),
     "fa2_device_status": (_I, [_P, _I]),
 }
@@ -82,6 +84,14 @@ def fa2_forward_splitkv(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, num_spl
     """Raw C call of the split-KV forward (caller-provided device workspace)."""
     return library().fa2_forward_splitkv(Q, K, V, O, LSE, B, H, Nq, Nk, d, int(bool(causal)), scale,
                                          num_splits, workspace, workspace_size, stream)
+
+
+def fa2_forward_splitkv_static(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, num_splits,
+                               stream) -> int:
+    """Raw C call of the split-KV forward that allocates nothing: its scratch
+    is the library's own 32 MiB device array (see include/fa2.h)."""
+    return library().fa2_forward_splitkv_static(Q, K, V, O, LSE, B, H, Nq, Nk, d,
+                                                int(bool(causal)), scale, num_splits, stream)
 
 
 def fa2_merge(O_parts, LSE_parts, num_parts, rows, d, O, LSE, stream) -> int:

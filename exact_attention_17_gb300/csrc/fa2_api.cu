@@ -296,6 +296,7 @@ extern "C" const char* fa2_status_string(int status) {
     case FA2_ERR_SCALE: return "scale must be finite and > 0";
     case FA2_ERR_MEMORY: return "a pointer is not device memory or its buffer is too small";
     case FA2_ERR_DEVICE: return "no usable sm_103 device is current";
+    case FA2_ERR_SCRATCH: return "the problem needs more split-KV scratch than the library's 32 MiB static buffer";
     default: return "unknown status";
   }
 }
@@ -309,4 +310,67 @@ extern "C" int fa2_device_status(fa2_stream_t stream, int reset) {
     if (cudaMemcpyToSymbol(g_device_status, &z, sizeof z) != cudaSuccess) return FA2_ERR_LAUNCH;
   }
   return v ? FA2_ERR_TIMEOUT : FA2_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Split-KV forward whose scratch lives in the library, for callers that cannot
+// allocate device memory themselves (see fa2_forward_splitkv_static in fa2.h).
+//
+// The scratch is one file-scope device array.  Host code must not pass the
+// array's name to a kernel: on the host it is only a stand-in for the symbol.
+// Its device address is looked up once per device, with that device current,
+// by the first call on the device.  All calls share the array and it keeps
+// the last call's contents; nothing in it needs to start at zero, because the
+// partial-results kernel writes every entry the merge kernel reads.  Calls
+// whose kernels overlap on the GPU (different streams, or different host
+// threads) race on it.
+namespace {
+
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(32) << 20;  // 32 MiB
+
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kStaticScratchBytes];
+
+struct StaticScratch {
+  std::once_flag once;
+  void* ptr = nullptr;
+  cudaError_t err = cudaErrorNotReady;
+};
+StaticScratch g_static_scratch[kMaxDevices];
+
+}  // namespace
+
+extern "C" int fa2_forward_splitkv_static(const void* Q, const void* K, const void* V, float* O,
+                                          float* LSE, int B, int H, int Nq, int Nk, int d,
+                                          int causal, float scale, int num_splits,
+                                          fa2_stream_t stream) {
+  Problem pr;
+  int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr);
+  if (rc != FA2_OK || pr.empty) return rc;
+  if (num_splits < 1 || num_splits > kMaxSplits) return FA2_ERR_SHAPE;
+  int splits = 1, tps = 1;
+  split_plan(Nk, num_splits, &splits, &tps);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (splits == 1)
+    return launch_forward(Q, K, V, O, LSE, pr, causal, scale, 1, tps, nullptr, nullptr, s);
+  const size_t need = workspace_bytes(pr.BH, Nq, d, splits);
+  if (need > kStaticScratchBytes) return FA2_ERR_SCRATCH;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA2_ERR_DEVICE;
+  StaticScratch& st = g_static_scratch[dev];
+  std::call_once(st.once, [&] {
+    st.err = cudaGetSymbolAddress(&st.ptr, g_splitkv_scratch);
+  });
+  if (st.err != cudaSuccess || st.ptr == nullptr) return FA2_ERR_LAUNCH;
+
+  const size_t rows = static_cast<size_t>(pr.BH) * Nq;
+  float* O_part = static_cast<float*>(st.ptr);
+  float* LSE_part = reinterpret_cast<float*>(static_cast<char*>(st.ptr) +
+                                             align256(static_cast<size_t>(splits) * rows * d * 4));
+  rc = launch_forward(Q, K, V, O, LSE, pr, causal, scale, splits, tps, O_part, LSE_part, s);
+  if (rc != FA2_OK) return rc;
+  return fa2host::launch_combine(d, O_part, LSE_part, splits, static_cast<long long>(rows), O, LSE, s) ==
+                 cudaSuccess
+             ? FA2_OK
+             : FA2_ERR_LAUNCH;
 }

@@ -58,7 +58,8 @@ typedef enum {
   FA2_ERR_TIMEOUT = 6,  /* a kernel gave up waiting on an internal barrier */
   FA2_ERR_SCALE = 7,    /* scale not finite and > 0 */
   FA2_ERR_MEMORY = 8,   /* a pointer is not device memory, or its buffer is too small */
-  FA2_ERR_DEVICE = 9    /* no usable sm_103 device is current */
+  FA2_ERR_DEVICE = 9,   /* no usable sm_103 device is current */
+  FA2_ERR_SCRATCH = 10  /* split-KV scratch needed exceeds the library's static buffer */
 } fa2_status;
 
 /*
@@ -129,6 +130,33 @@ int fa2_forward_splitkv(const void *Q, const void *K, const void *V, float *O, f
  */
 int fa2_merge(const float *O_parts, const float *LSE_parts, int num_parts, long long rows, int d,
               float *O, float *LSE, fa2_stream_t stream);
+
+/*
+ * Split-KV forward that allocates nothing and needs no workspace from the
+ * caller.  The pages have no counterpart; it exists for callers that cannot
+ * allocate device memory where they call attention -- for example a plugin
+ * or custom operator inside a framework that owns all device memory and
+ * hands it no allocator, or a server that reserves its memory at start-up
+ * and forbids allocation while serving -- and so cannot supply the
+ * workspace fa2_forward_splitkv needs.
+ *
+ * Same arguments, results and errors as fa2_forward_splitkv without the
+ * workspace.  The partial results live in one 32 MiB device array inside
+ * the library (33554432 bytes, held on every device that loads the library
+ * until the process exits); a problem that needs more, i.e. whose
+ * fa2_splitkv_workspace_bytes(B, H, Nq, d, num_splits) for the ranges
+ * actually used exceeds 32 MiB, is rejected with FA2_ERR_SCRATCH and nothing
+ * is launched.  The first call on a device looks up the array's device
+ * address (with that device current); make that first call before any
+ * stream capture.  All calls share the array: calls whose kernels may
+ * overlap on the GPU (other streams, other host threads) race on it and
+ * must be serialised by the caller.  The array keeps the last call's
+ * contents; no call depends on them.  The function never calls cudaMalloc,
+ * cudaFree or any other allocating routine.
+ */
+int fa2_forward_splitkv_static(const void *Q, const void *K, const void *V, float *O, float *LSE,
+                               int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                               int num_splits, fa2_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char *fa2_status_string(int status);
