@@ -59,7 +59,8 @@ __device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits until the barrier phase with the given parity has completed.
 // Bounded: gives up after `timeout_ns` of wall time, or as soon as another
-// thread of the CTA has raised `*abort`.  Returns false when it gave up.
+// thread of the CTA has raised `*abort` (abort may be null: no early exit).
+// Returns false when it gave up.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
                                          uint64_t timeout_ns) {
   const uint32_t a = smem_addr(bar);
@@ -68,7 +69,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   for (uint32_t it = 1;; ++it) {
     if (bar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0u) {
-      if (*abort) return false;
+      if (abort != nullptr && *abort) return false;
       if (global_timer_ns() - t0 > timeout_ns) return false;
     }
   }

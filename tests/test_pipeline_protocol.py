@@ -1,7 +1,10 @@
 """Model check of the tensor-core kernel's barrier protocol (host-only).
 
 The forward kernel coordinates a TMA producer, one MMA-issuing thread and two
-softmax warpgroups through mbarriers.  This test restates that protocol in a
+softmax warpgroups through mbarriers.  TMEM state is tracked too: S of a
+sub-tile must not be overwritten before the P V product has read the P that
+the softmax wrote over it, and the softmax's rescale of O and the epilogue
+must see exactly the tiles accumulated so far.  This test restates that protocol in a
 small discrete-event model and runs it under many random interleavings
 (TMA copies finish in any order, MMAs finish in issue order, roles advance
 in random order).  It fails on:
@@ -12,6 +15,7 @@ in random order).  It fails on:
   phase the waiter means (the parity would be ambiguous);
 * a TMA copy into a ring slot whose previous contents were not released;
 * an MMA reading a slot that does not hold the load it expects;
+* a TMEM hazard on S/P or on the O accumulator (see above);
 * a deadlock.
 
 The model mirrors the producer, issuer and softmax loops of the kernel in
@@ -81,6 +85,10 @@ class Sim:
         self.tma_inflight = []                # (barrier, slot or None, load id, bytes)
         self.mma_queue = []                   # ops in issue order: ("mma", reads) | ("commit", bar)
         self.released = set()
+        self.tmem_s = [None, None]            # S/P columns of each sub-tile
+        self.o_tiles = [-1, -1]               # last tile whose P V is in O
+        self.thread_queues = {}               # issuing thread -> its ops in order
+        self.current = None                   # issuing thread of the next mma/commit
 
     # -------------------------------------------------------- async engines
     def tma_load(self, bar, slot, g):
@@ -97,19 +105,48 @@ class Sim:
             self.slot[slot] = ("ready", g)
         bar.complete_tx(nb)
 
-    def mma(self, reads):
+    def mma(self, reads, tmem=None):
+        """Queue an MMA reading ring slots; `tmem` = ("S", sub, j) writes S_sub of
+        tile j, ("PV", sub, j) reads P_sub of tile j (checked when it executes)."""
         for slot, g in reads:
             if self.slot[slot] != ("ready", g):
                 raise ProtocolError(f"MMA expects load {g} in slot {slot}, finds {self.slot[slot]}")
-        self.mma_queue.append(("mma", reads))
+        op = ("mma", reads, tmem, len(self.mma_queue), self.rng.random())
+        self.mma_queue.append(op)
+        self.thread_queues.setdefault(self.current, []).append(op)
 
     def commit(self, bar, release=None):
-        self.mma_queue.append(("commit", bar, release))
+        op = ("commit", bar, release, len(self.mma_queue), self.rng.random())
+        self.mma_queue.append(op)
+        self.thread_queues.setdefault(self.current, []).append(op)
 
     def finish_one_mma(self):
-        op = self.mma_queue.pop(0)
+        # MMAs of one issuing thread run in order; the tensor pipe interleaves
+        # the threads' streams arbitrarily (per-thread queues, random choice).
+        queues = [q for q in self.thread_queues.values() if q]
+        if queues:
+            q = self.rng.choice(queues)
+            op = q.pop(0)
+            self.mma_queue.remove(op)
+        else:
+            op = self.mma_queue.pop(0)
+        if op[0] == "mma" and op[2] is not None:
+            kind, sub, j = op[2]
+            state = self.tmem_s[sub]
+            if kind == "S":
+                # S_sub(j) overwrites P_sub(j-1): the PV that reads it must have run
+                if j > 0 and state != ("P-read", j - 1):
+                    raise ProtocolError(f"S{sub}({j}) executes while TMEM holds {state}")
+                self.tmem_s[sub] = ("S", j)
+            else:
+                if state != ("P", j):
+                    raise ProtocolError(f"PV{sub}({j}) executes while TMEM holds {state}")
+                if self.o_tiles[sub] != j - 1:
+                    raise ProtocolError(f"PV{sub}({j}) accumulates onto O holding tile {self.o_tiles[sub]}")
+                self.tmem_s[sub] = ("P-read", j)
+                self.o_tiles[sub] = j
         if op[0] == "commit":
-            _, bar, release = op
+            _, bar, release = op[:3]
             if release is not None:
                 slot, g = release
                 if self.slot[slot] != ("ready", g):
@@ -138,11 +175,11 @@ class Sim:
         n0, n1 = self.n
 
         def issue_s(sub, g):
-            self.mma([(g % S, g)])
+            self.mma([(g % S, g)], ("S", sub, g // 2))
             self.commit(self.s_full[sub])
 
         def issue_pv(sub, g):
-            self.mma([(g % S, g)])
+            self.mma([(g % S, g)], ("PV", sub, g // 2))
             self.commit(self.o_done[sub])
 
         while not self.q_full.done(0):
@@ -187,19 +224,31 @@ class Sim:
         for j in range(n):
             while not self.s_full[sub].done(j):
                 yield
+            if self.tmem_s[sub] != ("S", j):
+                raise ProtocolError(f"softmax{sub}({j}) reads TMEM holding {self.tmem_s[sub]}")
             yield
+            self.tmem_s[sub] = ("P", j)
             if j > 0 and self.rng.random() < self.rescale_prob:
                 while not self.o_done[sub].done(j - 1):
                     yield
+                # the rescale reads and writes O: it must hold tiles 0..j-1 exactly
+                if self.o_tiles[sub] != j - 1:
+                    raise ProtocolError(f"rescale at tile {j} sees O holding tile {self.o_tiles[sub]}")
             self.p_ready[sub].arrive()
         if n > 0:
             while not self.o_done[sub].done(n - 1):
                 yield
+            if self.o_tiles[sub] != n - 1:
+                raise ProtocolError(f"epilogue of sub-tile {sub} sees O holding tile {self.o_tiles[sub]}")
 
     # -------------------------------------------------------- scheduler
+    def issuers(self):
+        return {"issuer": self.issuer()}
+
     def run(self):
-        roles = {"producer": self.producer(), "issuer": self.issuer(),
-                 "softmax0": self.softmax(0), "softmax1": self.softmax(1)}
+        roles = {"producer": self.producer(), "softmax0": self.softmax(0),
+                 "softmax1": self.softmax(1)}
+        roles.update(self.issuers())
         steps = 0
         while roles or self.tma_inflight or self.mma_queue:
             steps += 1
@@ -213,6 +262,7 @@ class Sim:
             elif c == "mma":
                 self.finish_one_mma()
             else:
+                self.current = c
                 try:
                     next(roles[c])
                 except StopIteration:
