@@ -44,8 +44,7 @@ DEFAULT_WORKLOAD = "b1_h32_n16384_d128_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["exact_attention_17_gb300/csrc/fa2_fwd_sm103.cuh",
                   "exact_attention_17_gb300/csrc/ptx.cuh",
-                  "exact_attention_17_gb300/csrc/fa2_tc_d128.cu",
-                  "exact_attention_17_gb300/csrc/fa2_tc_d64.cu"]
+                  "exact_attention_17_gb300/csrc/fa2_tc_d128_bf16.cu"]
 
 
 def kernel_source_hash() -> str:
@@ -249,6 +248,9 @@ def main():
                     help="seconds of oracle work for the cpu_baseline field (0 = skip)")
     ap.add_argument("--reference-step-s", type=float, default=None,
                     help="oracle seconds per reference step (default: ~120 s over all steps)")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"], help="Q/K/V element type")
+    ap.add_argument("--out-dtype", default="fp32", choices=["fp32", "same"],
+                    help="O element type: fp32, or the Q/K/V type")
     ap.add_argument("--num-splits", type=int, default=1,
                     help="split the keys into this many ranges (split-KV forward + merge)")
     ap.add_argument("--heads", type=int, default=None,
@@ -281,9 +283,12 @@ def main():
     import exact_attention_17_gb300 as fa2
 
     # seeded inputs, generated on the host (same bits the oracle sees)
-    Qh, Kh, Vh = inputs.workload_inputs(w)
+    in_dtype = torch.float16 if args.dtype == "fp16" else torch.bfloat16
+    out_dtype = torch.float32 if args.out_dtype == "fp32" else in_dtype
+    Qh, Kh, Vh = inputs.make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.seed, w.qk_dist, w.qk_std, w.v_dist,
+                                 dtype=in_dtype)
     Q, K, V = Qh.to(dev), Kh.to(dev), Vh.to(dev)
-    O = torch.empty(w.B, w.H, w.Nq, w.d, device=dev)
+    O = torch.empty(w.B, w.H, w.Nq, w.d, device=dev, dtype=out_dtype)
     L = torch.empty(w.B, w.H, w.Nq, device=dev)
     stream = torch.cuda.Stream(device=dev)
     in_bytes = (Q.numel() + K.numel() + V.numel()) * 2
@@ -302,7 +307,7 @@ def main():
 
     def step(s):
         fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, out=O, lse=L, stream=s,
-                    num_splits=args.num_splits, workspace=workspace)
+                    num_splits=args.num_splits, workspace=workspace, out_dtype=out_dtype)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -343,7 +348,7 @@ def main():
 
     # end to end through the public call: pinned host inputs -> device -> forward -> host result
     Qp, Kp, Vp = Qh.pin_memory(), Kh.pin_memory(), Vh.pin_memory()
-    Op = torch.empty(O.shape, dtype=torch.float32).pin_memory()
+    Op = torch.empty(O.shape, dtype=out_dtype).pin_memory()
     Lp = torch.empty(L.shape, dtype=torch.float32).pin_memory()
 
     def e2e_step():
@@ -351,7 +356,7 @@ def main():
         K.copy_(Kp, non_blocking=True)
         V.copy_(Vp, non_blocking=True)
         fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, out=O, lse=L, stream=stream,
-                    num_splits=args.num_splits, workspace=workspace)
+                    num_splits=args.num_splits, workspace=workspace, out_dtype=out_dtype)
         Op.copy_(O, non_blocking=True)
         Lp.copy_(L, non_blocking=True)
 
@@ -369,7 +374,7 @@ def main():
         torch.cuda.synchronize(dev)
     e2e_ms = job_time_ms(e0.elapsed_time(e1), dist, dev)
     h2d = (Qp.numel() + Kp.numel() + Vp.numel()) * 2
-    d2h = (Op.numel() + Lp.numel()) * 4
+    d2h = Op.numel() * Op.element_size() + Lp.numel() * 4
 
     if rank != 0:
         if dist:
@@ -402,9 +407,10 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": args.dtype,
         "data": "synthetic",
-        "config": dict(workload_config(w, l2_note), num_splits=args.num_splits),
+        "config": dict(workload_config(w, l2_note), num_splits=args.num_splits,
+                       inputs=f"{args.dtype} BHSD", outputs=f"{'fp32' if args.out_dtype == 'fp32' else args.dtype} O, fp32 LSE"),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": {
             "bound": "tensor",

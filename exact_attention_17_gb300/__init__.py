@@ -24,6 +24,11 @@ FA2_ERR_SCALE = 7
 FA2_ERR_MEMORY = 8
 FA2_ERR_DEVICE = 9
 FA2_ERR_SCRATCH = 10
+FA2_ERR_DTYPE = 11
+
+FA2_DTYPE_BF16 = 0
+FA2_DTYPE_FP16 = 1
+FA2_DTYPE_FP32 = 2
 
 # Every function the C header declares, with its ctypes signature.
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -32,6 +37,7 @@ _Z, _LL = ctypes.c_size_t, ctypes.c_longlong
 SIGNATURES = {
     "fa2_forward": (_I, _FORWARD_ARGS),
     "fa2_forward_simt": (_I, _FORWARD_ARGS),
+    "fa2_forward_typed": (_I, _FORWARD_ARGS[:-1] + [_I, _I, _P]),
     "fa2_splitkv_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "fa2_forward_splitkv": (_I, _FORWARD_ARGS[:-1] + [_I, _P, _Z, _P]),
     "fa2_merge": (_I, [_P, _P, _I, _LL, _I, _P, _P, _P]),
@@ -67,6 +73,13 @@ def library() -> ctypes.CDLL:
 def fa2_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, stream) -> int:
     """Raw C call: pointers (ints) and sizes, returns the status code."""
     return library().fa2_forward(Q, K, V, O, LSE, B, H, Nq, Nk, d, int(bool(causal)), scale, stream)
+
+
+def fa2_forward_typed(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, qkv_dtype, o_dtype,
+                      stream) -> int:
+    """Raw C call with element types (FA2_DTYPE_*) for Q/K/V and for O."""
+    return library().fa2_forward_typed(Q, K, V, O, LSE, B, H, Nq, Nk, d, int(bool(causal)), scale,
+                                       qkv_dtype, o_dtype, stream)
 
 
 def fa2_forward_simt(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, stream) -> int:
@@ -116,11 +129,12 @@ def _stream_handle(stream):
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-            stream=None, impl: str = "tc", num_splits: int = 1, workspace=None):
+            stream=None, impl: str = "tc", num_splits: int = 1, workspace=None, out_dtype=None):
     """Attention forward on torch CUDA tensors.
 
-    q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; all contiguous on one device.
-    Returns (O fp32 [B,H,Nq,d], LSE fp32 [B,H,Nq]).  ``scale`` defaults to
+    q: [B,H,Nq,d]; k, v: [B,H,Nk,d]; all bf16 or all fp16, contiguous, on one
+    device.  Returns (O [B,H,Nq,d], LSE fp32 [B,H,Nq]); O is fp32 unless
+    ``out_dtype`` is the input dtype (then O is stored in that 16-bit type).  ``scale`` defaults to
     1/sqrt(d) rounded to float32.  ``impl="simt"`` runs the CUDA-core
     cross-check implementation instead of the tensor-core one.
     ``num_splits > 1`` runs the split-KV forward over that many key ranges;
@@ -128,9 +142,16 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     """
     import torch
 
+    in_dtype = q.dtype
+    if in_dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q must be bf16 or fp16")
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+        if t.dtype != in_dtype or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor of q's dtype")
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    if out_dtype not in (torch.float32, in_dtype):
+        raise ValueError("out_dtype must be fp32 or the input dtype")
+    typed = in_dtype != torch.bfloat16 or out_dtype != torch.float32
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
@@ -138,16 +159,22 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     if scale is None:
         scale = float(torch.tensor(d, dtype=torch.float64).rsqrt().float())
     if out is None:
-        out = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device)
+        out = torch.empty((B, H, Nq, d), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    for name, t, shape in (("out", out, (B, H, Nq, d)), ("lse", lse, (B, H, Nq))):
-        if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
-            raise ValueError(f"{name} must be a contiguous fp32 tensor of shape {shape} on {q.device}")
+    for name, t, shape, dt in (("out", out, (B, H, Nq, d), out_dtype), ("lse", lse, (B, H, Nq), torch.float32)):
+        if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shape} on {q.device}")
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
             B, H, Nq, Nk, d, causal, float(scale))
+    codes = {torch.bfloat16: FA2_DTYPE_BF16, torch.float16: FA2_DTYPE_FP16, torch.float32: FA2_DTYPE_FP32}
     with torch.cuda.device(q.device):
-        if num_splits > 1:
+        if typed:
+            if impl != "tc" or num_splits > 1:
+                raise ValueError("fp16 inputs and 16-bit outputs run on the single-pass tensor-core path")
+            rc = fa2_forward_typed(*args, codes[in_dtype], codes[out_dtype], _stream_handle(stream))
+            name = "fa2_forward_typed"
+        elif num_splits > 1:
             if impl != "tc":
                 raise ValueError("split-KV runs on the tensor-core path only")
             need = fa2_splitkv_workspace_bytes(B, H, Nq, d, num_splits)

@@ -64,7 +64,8 @@ int device_ready() {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return;
     if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return;
     if (major != 10 || minor != 3) return;
-    if (fa2host::prepare_tc_d64() != cudaSuccess || fa2host::prepare_tc_d128() != cudaSuccess ||
+    if (fa2host::prepare_tc_d64_bf16() != cudaSuccess || fa2host::prepare_tc_d128_bf16() != cudaSuccess ||
+        fa2host::prepare_tc_d64_f16() != cudaSuccess || fa2host::prepare_tc_d128_f16() != cudaSuccess ||
         fa2host::prepare_simt() != cudaSuccess)
       return;
     st.usable = true;
@@ -89,15 +90,17 @@ bool device_range_ok(const void* p, size_t bytes) {
   return begin >= base && bytes <= size && begin - base <= size - bytes;
 }
 
-// 3-D bf16 map over [BH][N][d]: box = 64 columns (128 B, one swizzle atom) x 128 rows x 1.
-// Rows past N read as zero instead of running into the next head.
-bool encode_map(CUtensorMap* map, const void* base, int d, int N, int BH) {
+// 3-D map over [BH][N][d] 16-bit elements (bf16 or fp16): box = 64 columns
+// (128 B, one swizzle atom) x 128 rows x 1.  Rows past N read as zero
+// instead of running into the next head.
+bool encode_map(CUtensorMap* map, const void* base, int d, int N, int BH, bool f16) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = driver().encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  CUresult r = driver().encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                               3, const_cast<void*>(base), dims,
                                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -110,8 +113,8 @@ struct Problem {
   bool empty;
 };
 
-int validate(const void* Q, const void* K, const void* V, const float* O, const float* LSE, int B,
-             int H, int Nq, int Nk, int d, float scale, Problem* pr) {
+int validate(const void* Q, const void* K, const void* V, const void* O, const float* LSE, int B,
+             int H, int Nq, int Nk, int d, float scale, Problem* pr, size_t o_elem_bytes = 4) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA2_ERR_SHAPE;
   pr->B = B; pr->H = H; pr->Nq = Nq; pr->Nk = Nk; pr->d = d;
   pr->BH = static_cast<long long>(B) * H;
@@ -130,7 +133,7 @@ int validate(const void* Q, const void* K, const void* V, const float* O, const 
   const size_t bh = static_cast<size_t>(pr->BH);
   const size_t q_elems = bh * Nq * d, kv_elems = bh * Nk * d;
   if (!device_range_ok(Q, q_elems * 2) || !device_range_ok(K, kv_elems * 2) ||
-      !device_range_ok(V, kv_elems * 2) || !device_range_ok(O, q_elems * 4) ||
+      !device_range_ok(V, kv_elems * 2) || !device_range_ok(O, q_elems * o_elem_bytes) ||
       !device_range_ok(LSE, bh * Nq * 4))
     return FA2_ERR_MEMORY;
   return FA2_OK;
@@ -142,15 +145,16 @@ constexpr float kLog2e = 1.4426950408889634f;
 // tiles each (splits == 1: the whole key range, outputs O and LSE directly).
 int launch_forward(const void* Q, const void* K, const void* V, float* O, float* LSE,
                    const Problem& pr, int causal, float scale, int splits, int tiles_per_split,
-                   float* O_part, float* LSE_part, cudaStream_t s) {
+                   float* O_part, float* LSE_part, cudaStream_t s, bool f16 = false,
+                   bool o_half = false) {
   const int Nq = pr.Nq, Nk = pr.Nk, d = pr.d;
   const long long pairs = (static_cast<long long>(Nq) + 255) / 256;
   if (pairs * pr.BH * splits > 0x7fffffffLL) return FA2_ERR_SHAPE;
 
   CUtensorMap mq, mk, mv;
-  if (!encode_map(&mq, Q, d, Nq, static_cast<int>(pr.BH)) ||
-      !encode_map(&mk, K, d, Nk, static_cast<int>(pr.BH)) ||
-      !encode_map(&mv, V, d, Nk, static_cast<int>(pr.BH)))
+  if (!encode_map(&mq, Q, d, Nq, static_cast<int>(pr.BH), f16) ||
+      !encode_map(&mk, K, d, Nk, static_cast<int>(pr.BH), f16) ||
+      !encode_map(&mv, V, d, Nk, static_cast<int>(pr.BH), f16))
     return FA2_ERR_SHAPE;
 
   fa2dev::FwdParams p;
@@ -166,12 +170,19 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   p.tiles_per_split = tiles_per_split;
   p.O_part = O_part;
   p.LSE_part = LSE_part;
+  p.o_half = o_half ? 1 : 0;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
     return FA2_ERR_LAUNCH;
 
   const unsigned grid = static_cast<unsigned>(pairs * pr.BH * splits);
-  const cudaError_t e = d == 64 ? fa2host::launch_tc_d64(causal != 0, mq, mk, mv, p, grid, s)
-                                : fa2host::launch_tc_d128(causal != 0, mq, mk, mv, p, grid, s);
+  const bool c = causal != 0;
+  cudaError_t e;
+  if (d == 64)
+    e = f16 ? fa2host::launch_tc_d64_f16(c, mq, mk, mv, p, grid, s)
+            : fa2host::launch_tc_d64_bf16(c, mq, mk, mv, p, grid, s);
+  else
+    e = f16 ? fa2host::launch_tc_d128_f16(c, mq, mk, mv, p, grid, s)
+            : fa2host::launch_tc_d128_bf16(c, mq, mk, mv, p, grid, s);
   return e == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
 }
 
@@ -204,6 +215,20 @@ extern "C" int fa2_forward(const void* Q, const void* K, const void* V, float* O
   if (rc != FA2_OK || pr.empty) return rc;
   return launch_forward(Q, K, V, O, LSE, pr, causal, scale, 1, key_tiles(Nk), nullptr, nullptr,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fa2_forward_typed(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                 int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                 int qkv_dtype, int o_dtype, fa2_stream_t stream) {
+  if (qkv_dtype != FA2_DTYPE_BF16 && qkv_dtype != FA2_DTYPE_FP16) return FA2_ERR_DTYPE;
+  if (o_dtype != FA2_DTYPE_FP32 && o_dtype != qkv_dtype) return FA2_ERR_DTYPE;
+  const bool o_half = o_dtype != FA2_DTYPE_FP32;
+  Problem pr;
+  int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr, o_half ? 2 : 4);
+  if (rc != FA2_OK || pr.empty) return rc;
+  return launch_forward(Q, K, V, static_cast<float*>(O), LSE, pr, causal, scale, 1, key_tiles(Nk),
+                        nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream),
+                        qkv_dtype == FA2_DTYPE_FP16, o_half);
 }
 
 extern "C" size_t fa2_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
@@ -297,6 +322,7 @@ extern "C" const char* fa2_status_string(int status) {
     case FA2_ERR_MEMORY: return "a pointer is not device memory or its buffer is too small";
     case FA2_ERR_DEVICE: return "no usable sm_103 device is current";
     case FA2_ERR_SCRATCH: return "the problem needs more split-KV scratch than the library's 32 MiB static buffer";
+    case FA2_ERR_DTYPE: return "unsupported element types (Q/K/V bf16 or fp16; O fp32 or the Q/K/V type)";
     default: return "unknown status";
   }
 }

@@ -73,6 +73,8 @@ struct FwdParams {
   int tiles_per_split;
   float* O_part;
   float* LSE_part;
+  // O in the input element type (16 bits) instead of fp32 (num_splits == 1).
+  int o_half;
 };
 
 constexpr int kRowsPerSub = 128;   // tcgen05 M
@@ -131,7 +133,8 @@ __device__ __forceinline__ int kv_tiles_for(int u, int sub, int Nq, int t_begin,
   return max(0, stop - t_begin);
 }
 
-template <int D, bool CAUSAL>
+// F16: Q, K, V (and P) are fp16 instead of bf16.
+template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -241,8 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 9) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0 && nmax > 0) {
-        constexpr uint32_t kIdescS = idesc_bf16_f32(kRowsPerSub, kKeysPerTile, false, false);
-        constexpr uint32_t kIdescO = idesc_bf16_f32(kRowsPerSub, D, false, true);
+        constexpr uint32_t kIdescS = idesc_f32acc(kRowsPerSub, kKeysPerTile, false, false, F16);
+        constexpr uint32_t kIdescO = idesc_f32acc(kRowsPerSub, D, false, true, F16);
         const uint32_t sQaddr = smem_addr(sQ);
         const uint32_t sKVaddr = smem_addr(sKV);
 
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 t = __ffma2_rn(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), c2, o2);
           const float2 pe = make_float2(ex2_approx(t.x), ex2_approx(t.y));
           acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], pe);
-          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(pe.x, pe.y);
+          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_x2<F16>(pe.x, pe.y);
         }
         // the first half of P goes to TMEM while the second half is computed
         if (c == 1) tmem_st32(tS, pk[0]);
@@ -431,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t row_id = (static_cast<size_t>(p.num_splits > 1 ? split : 0) * p.BH + bh) * p.Nq + qi;
     float* orow = (p.num_splits > 1 ? p.O_part : p.O) + row_id * D;
     float* lse_out = (p.num_splits > 1 ? p.LSE_part : p.LSE) + row_id;
+    const bool half_out = p.o_half != 0 && p.num_splits == 1;
     if (n_tiles == 0 && store && p.num_splits > 1) {
       // no kept key in this range: contributes nothing to the merge
       for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -449,13 +453,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t o[32];
           tmem_ld32(tO + c * 32, o);
           tmem_ld_wait(o);
-          if (store) {
+          if (store && !half_out) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
               float4 v = make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
                                      __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
               *reinterpret_cast<float4*>(orow + c * 32 + e) = v;
             }
+          } else if (store) {
+            // O in the input element type: 32 values -> 64 bytes
+            uint32_t h[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              h[e >> 1] = pack_x2<F16>(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.O) + row_id * D + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
           }
         }
         if (store) *lse_out = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;

@@ -11,16 +11,21 @@
 namespace fa2host {
 
 // Raise the dynamic shared-memory limit of every kernel in the unit (current device).
-cudaError_t prepare_tc_d64();
-cudaError_t prepare_tc_d128();
+cudaError_t prepare_tc_d64_bf16();
+cudaError_t prepare_tc_d128_bf16();
+cudaError_t prepare_tc_d64_f16();
+cudaError_t prepare_tc_d128_f16();
 cudaError_t prepare_simt();
 
-cudaError_t launch_tc_d64(bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
-                          const CUtensorMap& mv, const fa2dev::FwdParams& p, unsigned grid,
-                          cudaStream_t s);
-cudaError_t launch_tc_d128(bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
-                           const CUtensorMap& mv, const fa2dev::FwdParams& p, unsigned grid,
-                           cudaStream_t s);
+#define FA2_DECLARE_TC_LAUNCH(name)                                                          \
+  cudaError_t name(bool causal, const CUtensorMap& mq, const CUtensorMap& mk,                \
+                   const CUtensorMap& mv, const fa2dev::FwdParams& p, unsigned grid,         \
+                   cudaStream_t s);
+FA2_DECLARE_TC_LAUNCH(launch_tc_d64_bf16)
+FA2_DECLARE_TC_LAUNCH(launch_tc_d128_bf16)
+FA2_DECLARE_TC_LAUNCH(launch_tc_d64_f16)
+FA2_DECLARE_TC_LAUNCH(launch_tc_d128_f16)
+#undef FA2_DECLARE_TC_LAUNCH
 cudaError_t launch_simt(int d, bool causal, const fa2dev::SimtParams& p, dim3 grid, cudaStream_t s);
 
 // Merge of S partial results (normalised O [S, R, d], LSE [S, R]) into O [R, d], LSE [R].

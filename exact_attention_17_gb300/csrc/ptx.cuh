@@ -157,12 +157,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulate.
-// a_mn / b_mn select MN-major (transposed) operands.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+// Instruction descriptor for kind::f16 with fp32 accumulate; A and B are
+// both bf16 (f16 = false) or both fp16 (f16 = true).  a_mn / b_mn select
+// MN-major (transposed) operands.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn, bool b_mn, bool f16) {
   return (1u << 4)                                  // D format: f32
-         | (1u << 7)                                // A format: bf16
-         | (1u << 10)                               // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)                   // A format: f16 = 0, bf16 = 1
+         | ((f16 ? 0u : 1u) << 10)                  // B format
          | (static_cast<uint32_t>(a_mn) << 15)      // A major
          | (static_cast<uint32_t>(b_mn) << 16)      // B major
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
@@ -281,6 +282,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two floats -> packed f16x2 (round to nearest even); `lo` lands in bits 0..15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_x2(float lo, float hi) {
+  if constexpr (F16)
+    return pack_f16x2(lo, hi);
+  else
+    return pack_bf16x2(lo, hi);
 }
 
 }  // namespace fa2dev

@@ -1,6 +1,6 @@
 """Seeded synthetic inputs for the attention forward pass.
 
-This module draws random numbers and rounds them to bf16; it holds none of
+This module draws random numbers and rounds them to bf16 or fp16; it holds none of
 the attention arithmetic.  It is the one module that both the CUDA path's
 callers (tests, benchmark) and the oracle's callers use, so that both sides
 see the same bf16 bit patterns.
@@ -16,7 +16,8 @@ Recipe (the pages measure on no dataset; these tensors stand in for the
   number of threads or on the machine;
 * "normal(std)" draws float32 standard normals times std, "uniform" draws
   float32 U[0, 1) mapped to [-1, 1);
-* the float32 samples are rounded to bf16 with round-to-nearest-even.
+* the float32 samples are rounded to bf16 (or, on request, fp16) with
+  round-to-nearest-even.
 """
 from __future__ import annotations
 
@@ -96,8 +97,9 @@ def _fill_chunk(out: np.ndarray, seed: int, tensor_id: int, chunk: int, dist: st
 
 
 def draw_bf16(shape, seed: int, tensor_id: int, dist: str = "normal", std: float = 1.0,
-              threads: int | None = None) -> torch.Tensor:
-    """One seeded tensor of the given shape, rounded to bf16 (CPU, contiguous)."""
+              threads: int | None = None, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """One seeded tensor of the given shape, rounded (nearest even) to `dtype`,
+    bf16 by default or fp16 (CPU, contiguous)."""
     n = int(np.prod(shape)) if len(shape) else 1
     buf = np.empty(n, dtype=np.float32)
     nchunks = (n + CHUNK - 1) // CHUNK
@@ -109,15 +111,16 @@ def draw_bf16(shape, seed: int, tensor_id: int, dist: str = "normal", std: float
     else:
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda job: _fill_chunk(job[1], seed, tensor_id, job[0], dist, std), jobs))
-    return torch.from_numpy(buf).to(torch.bfloat16).reshape(shape)
+    return torch.from_numpy(buf).to(dtype).reshape(shape)
 
 
 def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int, seed: int, qk_dist: str = "normal",
-             qk_std: float = 1.0, v_dist: str = "normal", threads: int | None = None):
-    """Q [B,H,Nq,d], K and V [B,H,Nk,d] as bf16 CPU tensors drawn from ``seed``."""
-    Q = draw_bf16((B, H, Nq, d), seed, 0, qk_dist, qk_std, threads)
-    K = draw_bf16((B, H, Nk, d), seed, 1, qk_dist, qk_std, threads)
-    V = draw_bf16((B, H, Nk, d), seed, 2, v_dist, 1.0, threads)
+             qk_std: float = 1.0, v_dist: str = "normal", threads: int | None = None,
+             dtype: torch.dtype = torch.bfloat16):
+    """Q [B,H,Nq,d], K and V [B,H,Nk,d] as bf16 (or fp16) CPU tensors drawn from ``seed``."""
+    Q = draw_bf16((B, H, Nq, d), seed, 0, qk_dist, qk_std, threads, dtype)
+    K = draw_bf16((B, H, Nk, d), seed, 1, qk_dist, qk_std, threads, dtype)
+    V = draw_bf16((B, H, Nk, d), seed, 2, v_dist, 1.0, threads, dtype)
     return Q, K, V
 
 
@@ -126,7 +129,7 @@ def workload_inputs(w: Workload, threads: int | None = None):
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
-    """The raw bf16 bit patterns of a CPU bf16 tensor, as a uint16 array (no copy)."""
-    if t.dtype != torch.bfloat16:
-        raise TypeError("expected a bf16 tensor")
+    """The raw bit patterns of a CPU bf16 (or fp16) tensor, as a uint16 array (no copy)."""
+    if t.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("expected a bf16 or fp16 tensor")
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -59,8 +59,12 @@ typedef enum {
   FA2_ERR_SCALE = 7,    /* scale not finite and > 0 */
   FA2_ERR_MEMORY = 8,   /* a pointer is not device memory, or its buffer is too small */
   FA2_ERR_DEVICE = 9,   /* no usable sm_103 device is current */
-  FA2_ERR_SCRATCH = 10  /* split-KV scratch needed exceeds the library's static buffer */
+  FA2_ERR_SCRATCH = 10, /* split-KV scratch needed exceeds the library's static buffer */
+  FA2_ERR_DTYPE = 11    /* unsupported element type combination */
 } fa2_status;
+
+/* Element types for fa2_forward_typed. */
+typedef enum { FA2_DTYPE_BF16 = 0, FA2_DTYPE_FP16 = 1, FA2_DTYPE_FP32 = 2 } fa2_dtype;
 
 /*
  * FlashAttention-2 forward on the tensor cores (tcgen05 MMAs accumulating in
@@ -77,6 +81,20 @@ typedef enum {
  */
 int fa2_forward(const void *Q, const void *K, const void *V, float *O, float *LSE, int B, int H,
                 int Nq, int Nk, int d, int causal, float scale, fa2_stream_t stream);
+
+/*
+ * fa2_forward with a choice of element types: Q, K, V are bf16 or fp16
+ * (qkv_dtype = FA2_DTYPE_BF16 / FA2_DTYPE_FP16, the same for all three); O is
+ * fp32 (o_dtype = FA2_DTYPE_FP32) or the Q/K/V type (o_dtype = qkv_dtype: O
+ * in the input dtype, as the "Triton内核实战" wrapper returns it).  LSE is
+ * always fp32.  With fp16 inputs P is rounded to fp16 for the P V product.
+ * Other combinations return FA2_ERR_DTYPE.  Layouts, sizes, limits and other
+ * errors as fa2_forward; a 16-bit O must be 16-byte aligned and hold
+ * B*H*Nq*d elements.
+ */
+int fa2_forward_typed(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                      int H, int Nq, int Nk, int d, int causal, float scale, int qkv_dtype,
+                      int o_dtype, fa2_stream_t stream);
 
 /*
  * The same operation on the CUDA cores, fp32 arithmetic, one thread per query

@@ -60,14 +60,29 @@ class Oracle:
         lib.oracle_attention.restype = ctypes.c_int
         lib.oracle_attention.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_int,
                                          ctypes.c_float, p, p, ctypes.c_int]
+        self.typed = hasattr(lib, "oracle_attention_rows_typed")
+        if self.typed:
+            lib.oracle_attention_rows_typed.restype = ctypes.c_int
+            lib.oracle_attention_rows_typed.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_int,
+                                                        ctypes.c_float, ctypes.c_int, p, i64, p, p,
+                                                        ctypes.c_int]
+            lib.oracle_widen.restype = ctypes.c_double
+            lib.oracle_widen.argtypes = [ctypes.c_uint16, ctypes.c_int]
         self.lib = lib
         self.path = lib_path
 
-    def attention(self, Q, K, V, causal: bool, scale: float, nthreads: int | None = None):
-        """Exact attention of every row.  Q [B,H,Nq,d], K/V [B,H,Nk,d] bf16 bits.
+    def attention(self, Q, K, V, causal: bool, scale: float, nthreads: int | None = None,
+                  dtype: str = "bf16"):
+        """Exact attention of every row.  Q [B,H,Nq,d], K/V [B,H,Nk,d] 16-bit
+        patterns of `dtype` ("bf16" or "fp16").
 
         Returns (O [B,H,Nq,d] float64, LSE [B,H,Nq] float64).
         """
+        if dtype != "bf16":
+            B, H, Nq = np.shape(Q)[:3]
+            d = np.shape(Q)[3]
+            O, L = self.attention_rows(Q, K, V, causal, scale, np.arange(B * H * Nq), nthreads, dtype)
+            return O.reshape(B, H, Nq, d), L.reshape(B, H, Nq)
         Q, K, V = _bits(Q), _bits(K), _bits(V)
         B, H, Nq, d = Q.shape
         Nk = K.shape[2]
@@ -83,7 +98,7 @@ class Oracle:
         return O, LSE
 
     def attention_rows(self, Q, K, V, causal: bool, scale: float, rows,
-                       nthreads: int | None = None):
+                       nthreads: int | None = None, dtype: str = "bf16"):
         """Exact attention of selected rows.
 
         ``rows`` holds flattened row ids (b*H + h)*Nq + i.  Returns
@@ -98,12 +113,27 @@ class Oracle:
         n = rows.shape[0]
         O = np.empty((n, d), dtype=np.float64)
         LSE = np.empty((n,), dtype=np.float64)
-        rc = self.lib.oracle_attention_rows(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d,
-                                            int(bool(causal)), float(scale), _ptr(rows), n,
-                                            _ptr(O), _ptr(LSE), nthreads or default_threads())
+        code = _DTYPES[dtype]
+        if code == 0 and not self.typed:
+            rc = self.lib.oracle_attention_rows(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d,
+                                                int(bool(causal)), float(scale), _ptr(rows), n,
+                                                _ptr(O), _ptr(LSE), nthreads or default_threads())
+        else:
+            rc = self.lib.oracle_attention_rows_typed(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d,
+                                                      int(bool(causal)), float(scale), code,
+                                                      _ptr(rows), n, _ptr(O), _ptr(LSE),
+                                                      nthreads or default_threads())
         if rc != 0:
             raise ValueError(f"oracle_attention_rows failed with code {rc}")
         return O, LSE
+
+
+    def widen(self, bits: int, dtype: str) -> float:
+        """The oracle's exact widening of one 16-bit pattern to double."""
+        return self.lib.oracle_widen(bits, _DTYPES[dtype])
+
+
+_DTYPES = {"bf16": 0, "fp16": 1}
 
 
 def compile_source(src_path: str, out_path: str) -> str:
@@ -136,14 +166,20 @@ def default_threads() -> int:
     return os.cpu_count() or 1
 
 
-def attention(Q, K, V, causal: bool, scale: float, nthreads: int | None = None):
+def attention(Q, K, V, causal: bool, scale: float, nthreads: int | None = None, dtype: str = "bf16"):
     """Exact attention of every row (see ``Oracle.attention``)."""
-    return _default().attention(Q, K, V, causal, scale, nthreads)
+    return _default().attention(Q, K, V, causal, scale, nthreads, dtype)
 
 
-def attention_rows(Q, K, V, causal: bool, scale: float, rows, nthreads: int | None = None):
+def attention_rows(Q, K, V, causal: bool, scale: float, rows, nthreads: int | None = None,
+                   dtype: str = "bf16"):
     """Exact attention of selected rows (see ``Oracle.attention_rows``)."""
-    return _default().attention_rows(Q, K, V, causal, scale, rows, nthreads)
+    return _default().attention_rows(Q, K, V, causal, scale, rows, nthreads, dtype)
+
+
+def widen(bits: int, dtype: str) -> float:
+    """The oracle's exact widening of one 16-bit pattern (see ``Oracle.widen``)."""
+    return _default().widen(bits, dtype)
 
 
 def merge(O_parts, LSE_parts):

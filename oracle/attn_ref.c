@@ -18,7 +18,8 @@
  * page, "online softmax" paragraph: the block-wise l equals the one-shot sum).
  *
  * Readings taken where the pages are silent:
- *   - inputs are bf16 bit patterns; each is widened exactly to double, so the
+ *   - inputs are bf16 or fp16 bit patterns (fp16: the input dtype of the
+ *     "Triton内核实战" wrapper); each is widened exactly to double, so the
  *     oracle sees the same rounded values the GPU sees;
  *   - scale is the caller's float, widened (not recomputed as 1/sqrt(d));
  *   - causal masking is top-left aligned: row i keeps keys j <= i (and j < Nk).
@@ -45,10 +46,37 @@ static double bf16_bits_to_double(uint16_t bits)
     return (double)f;
 }
 
+/* Exact widening of an IEEE 754 binary16 bit pattern: 1 sign bit, 5 exponent
+ * bits (bias 15), 10 fraction bits; exponent 0 encodes zero and subnormals
+ * (fraction * 2^-24), exponent 31 encodes infinities and NaNs. */
+static double fp16_bits_to_double(uint16_t bits)
+{
+    const int sign = (bits >> 15) & 1;
+    const int exponent = (bits >> 10) & 0x1f;
+    const int fraction = bits & 0x3ff;
+    double v;
+    if (exponent == 0)
+        v = ldexp((double)fraction, -24);
+    else if (exponent == 31)
+        v = fraction ? NAN : INFINITY;
+    else
+        v = ldexp((double)(fraction | 0x400), exponent - 25);
+    return sign ? -v : v;
+}
+
+/* Input element types. */
+enum { ORACLE_BF16 = 0, ORACLE_FP16 = 1 };
+
+static double widen(uint16_t bits, int dtype)
+{
+    return dtype == ORACLE_FP16 ? fp16_bits_to_double(bits) : bf16_bits_to_double(bits);
+}
+
 typedef struct {
     const uint16_t *Q, *K, *V;
     int64_t H, Nq, Nk, d;
     int causal;
+    int dtype;
     double scale;
     const int64_t *rows;    /* flattened (b*H + h)*Nq + i; NULL = all rows */
     int64_t nrows;
@@ -78,7 +106,7 @@ static void attend_one_row(const oracle_job *J, int64_t flat, double *s,
     for (int64_t j = 0; j < n; ++j) {
         double acc = 0.0;
         for (int64_t c = 0; c < d; ++c)
-            acc += bf16_bits_to_double(q[c]) * bf16_bits_to_double(kb[j * d + c]);
+            acc += widen(q[c], J->dtype) * widen(kb[j * d + c], J->dtype);
         s[j] = J->scale * acc;
         if (s[j] > m)
             m = s[j];
@@ -95,7 +123,7 @@ static void attend_one_row(const oracle_job *J, int64_t flat, double *s,
     for (int64_t j = 0; j < n; ++j) {
         const double w = exp(s[j] - m) / l;
         for (int64_t c = 0; c < d; ++c)
-            o[c] += w * bf16_bits_to_double(vb[j * d + c]);
+            o[c] += w * widen(vb[j * d + c], J->dtype);
     }
     *lse = m + log(l);
 }
@@ -133,12 +161,14 @@ static void *oracle_worker(void *arg)
  * Returns 0 on success, 1 on a bad argument (including a row id out of
  * range or Nk < 1), 2 if a worker could not allocate its score buffer.
  */
-int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                          int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
-                          int causal, float scale, const int64_t *rows, int64_t nrows,
-                          double *O, double *LSE, int nthreads)
+int oracle_attention_rows_typed(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                                int causal, float scale, int dtype, const int64_t *rows,
+                                int64_t nrows, double *O, double *LSE, int nthreads)
 {
     if (!Q || !K || !V || !O || !LSE || B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || nrows < 0)
+        return 1;
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16)
         return 1;
     const int64_t total = B * H * Nq;
     if (!rows && nrows != total)
@@ -154,6 +184,7 @@ int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *
     J.Q = Q; J.K = K; J.V = V;
     J.H = H; J.Nq = Nq; J.Nk = Nk; J.d = d;
     J.causal = causal ? 1 : 0;
+    J.dtype = dtype;
     J.scale = (double)scale;
     J.rows = rows; J.nrows = nrows;
     J.O = O; J.LSE = LSE;
@@ -174,6 +205,22 @@ int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *
     for (int t = 0; t < started; ++t)
         pthread_join(tid[t], NULL);
     return J.error ? 2 : 0;
+}
+
+/* bf16 inputs (the original entry point). */
+int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                          int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                          int causal, float scale, const int64_t *rows, int64_t nrows,
+                          double *O, double *LSE, int nthreads)
+{
+    return oracle_attention_rows_typed(Q, K, V, B, H, Nq, Nk, d, causal, scale, ORACLE_BF16,
+                                       rows, nrows, O, LSE, nthreads);
+}
+
+/* Widened value of one 16-bit pattern (exposed for the widening pins). */
+double oracle_widen(uint16_t bits, int dtype)
+{
+    return widen(bits, dtype);
 }
 
 /* Every row of every (b, h): O [B,H,Nq,d], LSE [B,H,Nq]. */

@@ -81,3 +81,13 @@ def test_host_side_argument_errors(lib, fn):
     for name in ("Q", "K", "V", "O"):
         assert c(**{name: 24}) == fa2.FA2_ERR_ALIGN
     assert c(LSE=18) == fa2.FA2_ERR_ALIGN
+
+
+def test_typed_entry_point_rejects_bad_element_types_on_the_host(lib):
+    args = (16, 16, 16, 16, 16, 1, 1, 8, 8, 64, 0, 0.125)
+    assert fa2.fa2_forward_typed(*args, fa2.FA2_DTYPE_FP32, fa2.FA2_DTYPE_FP32, None) == fa2.FA2_ERR_DTYPE
+    assert fa2.fa2_forward_typed(*args, fa2.FA2_DTYPE_BF16, fa2.FA2_DTYPE_FP16, None) == fa2.FA2_ERR_DTYPE
+    assert fa2.fa2_forward_typed(*args, fa2.FA2_DTYPE_FP16, fa2.FA2_DTYPE_BF16, None) == fa2.FA2_ERR_DTYPE
+    # valid types, empty problem: nothing launched
+    empty = (16, 16, 16, 16, 16, 0, 1, 8, 8, 64, 0, 0.125)
+    assert fa2.fa2_forward_typed(*empty, fa2.FA2_DTYPE_FP16, fa2.FA2_DTYPE_FP16, None) == fa2.FA2_OK

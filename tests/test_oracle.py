@@ -350,16 +350,40 @@ MUTANTS = {
     "lse_max_dropped": ("*lse = m + log(l);", "*lse = log(l);"),
     "lse_log_dropped": ("*lse = m + log(l);", "*lse = m;"),
     "v_rows_reversed": ("vb[j * d + c]", "vb[(n - 1 - j) * d + c]"),
-    "q_transposed": ("bf16_bits_to_double(q[c])", "bf16_bits_to_double(q[d - 1 - c])"),
+    "q_transposed": ("widen(q[c], J->dtype)", "widen(q[d - 1 - c], J->dtype)"),
+    "fp16_exponent_bias": ("exponent - 25", "exponent - 24"),
+    "fp16_subnormal_scale": ("ldexp((double)fraction, -24)", "ldexp((double)fraction, -25)"),
+    "fp16_implicit_bit": ("(fraction | 0x400)", "(fraction)"),
     "k_from_query_block": ("const uint16_t *kb = J->K + bh * J->Nk * d;",
                            "const uint16_t *kb = J->K + (bh > 0 ? bh - 1 : 0) * J->Nk * d;"),
     "widening_shift": ("((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
 }
 
 
+def check_fp16_widening(orc):
+    """Every finite binary16 pattern widens to the value torch's float16 -> float64
+    conversion gives (a library routine), and fp16 attention matches torch."""
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.float16).double().numpy()
+    finite = np.isfinite(ref)
+    got = np.array([orc.widen(int(b), "fp16") for b in bits[finite]])
+    assert np.array_equal(got, ref[finite])
+    rng = np.random.default_rng(14)
+    for causal in (False, True):
+        q, k, v = (rng.standard_normal(sh).astype(np.float16) for sh in ((1, 2, 9, 16), (1, 2, 12, 16), (1, 2, 12, 16)))
+        O, L = orc.attention(q.view(np.uint16), k.view(np.uint16), v.view(np.uint16), causal, 0.25, dtype="fp16")
+        qt, kt, vt = (torch.from_numpy(x.astype(np.float64)) for x in (q, k, v))
+        Ot = F.scaled_dot_product_attention(qt, kt, vt, is_causal=causal, scale=0.25).numpy()
+        assert np.max(np.abs(O - Ot)) < 1e-12
+
+
+def test_fp16_widening_and_attention(oracle_mod):
+    check_fp16_widening(oracle_mod)
+
+
 def all_pins(orc):
     for check in (check_worked_example, check_against_torch, check_closed_forms,
-                  check_invariants, check_lse_merge):
+                  check_invariants, check_lse_merge, check_fp16_widening):
         try:
             check(orc)
         except AssertionError:
