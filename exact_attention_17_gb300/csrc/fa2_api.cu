@@ -52,6 +52,7 @@ const DriverFns& driver() {
 struct DeviceState {
   std::once_flag once;
   bool usable = false;
+  int sms = 0;
 };
 DeviceState g_devices[kMaxDevices];
 
@@ -64,6 +65,7 @@ int device_ready() {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return;
     if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return;
     if (major != 10 || minor != 3) return;
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return;
     if (fa2host::prepare_tc_d64_bf16() != cudaSuccess || fa2host::prepare_tc_d128_bf16() != cudaSuccess ||
         fa2host::prepare_tc_d64_f16() != cudaSuccess || fa2host::prepare_tc_d128_f16() != cudaSuccess ||
         fa2host::prepare_simt() != cudaSuccess)
@@ -73,6 +75,13 @@ int device_ready() {
   if (!st.usable) return FA2_ERR_DEVICE;
   if (!driver().ok) return FA2_ERR_DEVICE;
   return FA2_OK;
+}
+
+// Streaming multiprocessors of the current device (after device_ready succeeded).
+int sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return g_devices[dev].sms > 0 ? g_devices[dev].sms : 148;
 }
 
 // The whole byte range [p, p + bytes) must be device memory of one allocation.
@@ -141,6 +150,16 @@ int validate(const void* Q, const void* K, const void* V, const void* O, const f
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Query sub-tiles of 128 rows per CTA.  Two (one CTA per SM, the sub-tiles
+// ping-pong on the tensor core) is faster for long query blocks; one (two
+// CTAs per SM) when a second sub-tile would have no rows (Nq <= 128) or when
+// two-sub-tile CTAs would not fill two waves of the GPU.
+int subtiles_per_cta(const Problem& pr, int splits) {
+  if (pr.Nq <= 128) return 1;
+  const long long ctas2 = (static_cast<long long>(pr.Nq) + 255) / 256 * pr.BH * splits;
+  return ctas2 < 2LL * sm_count() ? 1 : 2;
+}
+
 // Launch of the tensor-core kernel over `splits` key ranges of `tiles_per_split`
 // tiles each (splits == 1: the whole key range, outputs O and LSE directly).
 int launch_forward(const void* Q, const void* K, const void* V, float* O, float* LSE,
@@ -148,8 +167,9 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
                    float* O_part, float* LSE_part, cudaStream_t s, bool f16 = false,
                    bool o_half = false) {
   const int Nq = pr.Nq, Nk = pr.Nk, d = pr.d;
-  const long long pairs = (static_cast<long long>(Nq) + 255) / 256;
-  if (pairs * pr.BH * splits > 0x7fffffffLL) return FA2_ERR_SHAPE;
+  const int subs = subtiles_per_cta(pr, splits);
+  const long long blocks = (static_cast<long long>(Nq) + 128 * subs - 1) / (128 * subs);
+  if (blocks * pr.BH * splits > 0x7fffffffLL) return FA2_ERR_SHAPE;
 
   CUtensorMap mq, mk, mv;
   if (!encode_map(&mq, Q, d, Nq, static_cast<int>(pr.BH), f16) ||
@@ -163,7 +183,7 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   p.Nq = Nq;
   p.Nk = Nk;
   p.BH = static_cast<int>(pr.BH);
-  p.q_pairs = static_cast<int>(pairs);
+  p.q_blocks = static_cast<int>(blocks);
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = kWaitTimeoutNs;
   p.num_splits = splits;
@@ -174,15 +194,15 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
     return FA2_ERR_LAUNCH;
 
-  const unsigned grid = static_cast<unsigned>(pairs * pr.BH * splits);
+  const unsigned grid = static_cast<unsigned>(blocks * pr.BH * splits);
   const bool c = causal != 0;
   cudaError_t e;
   if (d == 64)
-    e = f16 ? fa2host::launch_tc_d64_f16(c, mq, mk, mv, p, grid, s)
-            : fa2host::launch_tc_d64_bf16(c, mq, mk, mv, p, grid, s);
+    e = f16 ? fa2host::launch_tc_d64_f16(subs, c, mq, mk, mv, p, grid, s)
+            : fa2host::launch_tc_d64_bf16(subs, c, mq, mk, mv, p, grid, s);
   else
-    e = f16 ? fa2host::launch_tc_d128_f16(c, mq, mk, mv, p, grid, s)
-            : fa2host::launch_tc_d128_bf16(c, mq, mk, mv, p, grid, s);
+    e = f16 ? fa2host::launch_tc_d128_f16(subs, c, mq, mk, mv, p, grid, s)
+            : fa2host::launch_tc_d128_bf16(subs, c, mq, mk, mv, p, grid, s);
   return e == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
 }
 

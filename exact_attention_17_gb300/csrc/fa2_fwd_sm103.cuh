@@ -21,11 +21,12 @@
 //
 // GB300 mapping (not from the pages):
 //  * one CTA = two 128-row Q sub-tiles (256 query rows) sharing one K/V
-//    stream; 12 warps: warps 0-3 and 4-7 are the softmax warpgroups of
-//    sub-tile 0 and 1 (thread t owns query row t = TMEM lane t, so row max and
-//    row sum need no cross-thread reduction -- the "sliced-Q" split of
-//    "Flash Attention 全解析(上)" section 3.2.2 taken to one row per thread);
-//    warp 8 issues TMA loads, warp 9 issues tcgen05 MMAs and owns TMEM;
+//    stream (or one sub-tile, with two CTAs per SM); warps 0-3 (and 4-7) are
+//    the softmax warpgroups of the sub-tiles (thread t owns query row t =
+//    TMEM lane t, so row max and row sum need no cross-thread reduction --
+//    the "sliced-Q" split of "Flash Attention 全解析(上)" section 3.2.2 taken to
+//    one row per thread); the next warp issues TMA loads, the one after it
+//    issues the tcgen05 MMAs and owns TMEM;
 //  * S = Q K^T runs as tcgen05.mma (bf16 x bf16 -> f32) from shared memory into
 //    TMEM; P is written back to TMEM as bf16 over S's columns and O += P V
 //    takes P straight from TMEM (A operand) and V from shared memory (MN-major);
@@ -59,7 +60,7 @@ struct FwdParams {
   int Nq;
   int Nk;
   int BH;
-  int q_pairs;     // ceil(Nq / 256)
+  int q_blocks;    // ceil(Nq / rows per CTA)
   float scale_log2;  // scale * log2(e)
   int* status;     // device status word
   unsigned long long timeout_ns;
@@ -79,25 +80,39 @@ struct FwdParams {
 
 constexpr int kRowsPerSub = 128;   // tcgen05 M
 constexpr int kKeysPerTile = 128;  // K/V block (N of S, K of P V)
-constexpr int kThreads = 384;
-// Register budgets after the start-up rebalancing: 168 per thread at launch
-// (65536 / 384, rounded down to a multiple of 8) = 64512 in total;
-// 2 x 128 x kRegsSoftmax + 128 x kRegsProducer = 63488 stays within it.
-constexpr int kRegsSoftmax = 216;
-constexpr int kRegsProducer = 64;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsProducer <= 168 * kThreads,
-              "register rebalancing exceeds the launch allocation");
+// A CTA holds SUBS query sub-tiles of 128 rows: SUBS = 2 (one CTA per SM,
+// the two sub-tiles ping-pong on the tensor core) or SUBS = 1 (two CTAs per
+// SM, each with its own MMA-issuing thread).  Threads: 128 per sub-tile
+// (softmax) plus one warpgroup for the producer and MMA warps.
+template <int SUBS>
+struct FwdShape {
+  static constexpr int kThreads = SUBS * 128 + 128;
+  static constexpr int kCtasPerSm = SUBS == 2 ? 1 : 2;
+  // Register budgets after the start-up rebalancing.  At launch every thread
+  // has kLaunch registers (65536 / (threads * CTAs per SM), rounded down to a
+  // multiple of 8); the softmax warpgroups then take kSoftmax and the
+  // producer warpgroup gives back down to kProducer.
+  static constexpr int kLaunch = SUBS == 2 ? 168 : 128;
+  static constexpr int kSoftmax = SUBS == 2 ? 216 : 208;
+  static constexpr int kProducer = SUBS == 2 ? 64 : 48;
+  static_assert(SUBS * 128 * kSoftmax + 128 * kProducer <= kLaunch * kThreads,
+                "register rebalancing exceeds the launch allocation");
+  static_assert(kLaunch * kThreads * kCtasPerSm <= 65536, "launch registers exceed the SM");
+};
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int D>
+template <int D, int SUBS>
 struct FwdConfig {
   static constexpr int kChunks = D / 64;                    // 128-byte swizzle atoms per row
   static constexpr uint32_t kTileBytes = kKeysPerTile * D * 2;  // one K or V tile, one Q sub-tile
-  static constexpr int kStages = D == 128 ? 4 : 8;          // K/V ring slots (K and V alternate)
-  static constexpr uint32_t kColsO0 = 256;
-  static constexpr uint32_t kColsO1 = 256 + D;
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kSmemData = (2 + kStages) * kTileBytes;
+  // K/V ring slots (K and V alternate); with two CTAs per SM each gets half
+  // of the shared memory.
+  static constexpr int kStages = SUBS == 2 ? (D == 128 ? 4 : 8) : (D == 128 ? 2 : 5);
+  // TMEM columns: S of each sub-tile (128 fp32 columns), then O of each (D).
+  static constexpr uint32_t kColsO0 = SUBS * 128;
+  static constexpr uint32_t kColsO1 = SUBS * 128 + D;
+  static constexpr uint32_t kTmemCols = SUBS == 2 ? 512 : 256;
+  static constexpr uint32_t kSmemData = (SUBS + kStages) * kTileBytes;
   static constexpr uint32_t kSmemBytes = kSmemData + 1024 /*align*/ + 1024 /*barriers*/;
 };
 
@@ -121,9 +136,9 @@ __device__ __forceinline__ void raise_abort(volatile int* abort, int* status) {
 
 // Number of K/V tiles query sub-tile `sub` of pair `u` visits within the key
 // tile range [t_begin, t_end) (0 = no rows, or every key masked).
-template <bool CAUSAL>
+template <bool CAUSAL, int SUBS>
 __device__ __forceinline__ int kv_tiles_for(int u, int sub, int Nq, int t_begin, int t_end) {
-  const int first = u * 2 * kRowsPerSub + sub * kRowsPerSub;
+  const int first = (u * SUBS + sub) * kRowsPerSub;
   if (first >= Nq) return 0;
   int stop = t_end;
   if (CAUSAL) {
@@ -133,13 +148,16 @@ __device__ __forceinline__ int kv_tiles_for(int u, int sub, int Nq, int t_begin,
   return max(0, stop - t_begin);
 }
 
-// F16: Q, K, V (and P) are fp16 instead of bf16.
-template <int D, bool CAUSAL, bool F16>
-__global__ void __launch_bounds__(kThreads, 1)
+// F16: Q, K, V (and P) are fp16 instead of bf16.  SUBS: query sub-tiles per CTA.
+template <int D, bool CAUSAL, bool F16, int SUBS>
+__global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCtasPerSm)
     fa2_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using Cfg = FwdConfig<D>;
+  using Cfg = FwdConfig<D, SUBS>;
+  using Shape = FwdShape<SUBS>;
+  constexpr int kWarpProducer = 4 * SUBS;      // TMA warp
+  constexpr int kWarpMma = 4 * SUBS + 1;       // MMA warp, owns the TMEM allocation
   constexpr int STAGES = Cfg::kStages;
   constexpr uint32_t TILE = Cfg::kTileBytes;
   constexpr int NCH = Cfg::kChunks;
@@ -148,8 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;                  // two sub-tiles
-  uint8_t* sKV = smem + 2 * TILE;      // STAGES tiles
+  uint8_t* sQ = smem;                  // SUBS sub-tiles
+  uint8_t* sKV = smem + SUBS * TILE;   // STAGES tiles
   auto* bars = reinterpret_cast<FwdBarriers<STAGES>*>(smem + Cfg::kSmemData);
   volatile int* abort = &bars->abort;
 
@@ -159,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Work item: (pair u of query sub-tiles, key range, b*H + h).  Pairs of one
   // head and range are adjacent so that concurrently running CTAs share K/V
   // tiles through L2; under the causal mask the heaviest pairs start first.
-  const int U = p.q_pairs;
+  const int U = p.q_blocks;
   const int item = blockIdx.x / U;
   const int bh = item / p.num_splits;
   const int split = item - bh * p.num_splits;
@@ -168,10 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int all_tiles = (p.Nk + kKeysPerTile - 1) / kKeysPerTile;
   const int t_begin = split * p.tiles_per_split;
   const int t_end = min(all_tiles, t_begin + p.tiles_per_split);
-  const int n0 = kv_tiles_for<CAUSAL>(u, 0, p.Nq, t_begin, t_end);
-  const int n1 = kv_tiles_for<CAUSAL>(u, 1, p.Nq, t_begin, t_end);
+  const int n0 = kv_tiles_for<CAUSAL, SUBS>(u, 0, p.Nq, t_begin, t_end);
+  const int n1 = SUBS == 2 ? kv_tiles_for<CAUSAL, SUBS>(u, 1, p.Nq, t_begin, t_end) : 0;
   const int nmax = max(n0, n1);
-  const int q_row0 = u * 2 * kRowsPerSub;
+  const int q_row0 = u * SUBS * kRowsPerSub;
 
   if (threadIdx.x == 0) {
     bar_init(&bars->q_full, 1);
@@ -188,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(&bars->tmem_base, Cfg::kTmemCols);
     tmem_relinquish();
     tc_fence_before_sync();
@@ -199,9 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Each role branch starts with its register budget change, so that the
   // compiler can allocate each branch for its own budget.
-  if (warp >= 8) {
-    regs_decrease<kRegsProducer>();
-    if (warp == 8) {
+  if (warp >= kWarpProducer) {
+    regs_decrease<Shape::kProducer>();
+    if (warp == kWarpProducer) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
         prefetch_tmap(&tm_q);
@@ -209,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_v);
         const uint32_t qbytes = (n0 > 0 ? TILE : 0u) + (n1 > 0 ? TILE : 0u);
         bar_arrive_expect_tx(&bars->q_full, qbytes);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < SUBS; ++s) {
           if ((s == 0 ? n0 : n1) == 0) continue;
           for (int c = 0; c < NCH; ++c)
             tma_load_3d(sQ + s * TILE + c * kChunkBytes, &tm_q, &bars->q_full, c * 64,
@@ -241,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = max(0, issued - STAGES); k < issued; ++k)
           wait_bar(&bars->kv_full[k % STAGES], (k / STAGES) & 1, &never, p.timeout_ns);
       }
-    } else if (warp == 9) {
+    } else if (warp == kWarpMma) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0 && nmax > 0) {
         constexpr uint32_t kIdescS = idesc_f32acc(kRowsPerSub, kKeysPerTile, false, false, F16);
@@ -316,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    regs_increase<kRegsSoftmax>();
+    regs_increase<Shape::kSoftmax>();
     // ------------------------------------------------------------ softmax
     const int sub = warp >> 2;
     const int n_tiles = sub == 0 ? n0 : n1;
@@ -480,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }

@@ -212,3 +212,25 @@ def test_rejects_host_and_undersized_memory(dev):
                          1, 2, big_n, big_n, d, 0, 0.125, None)
     assert rc == fa2.FA2_ERR_MEMORY
     torch.cuda.synchronize()
+
+
+# Shapes whose grid of 256-row CTAs fills two waves of the GPU, so the library
+# runs them with two query sub-tiles per CTA (smaller grids use one): ragged
+# last blocks, a one-row second sub-tile, short key ranges.
+TWO_SUBTILE_EDGE = [(1, 64, 1200, 1200), (1, 152, 257, 300), (2, 51, 513, 129), (1, 160, 511, 64)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("B,H,Nq,Nk", TWO_SUBTILE_EDGE)
+def test_edge_sizes_two_subtile_grid(dev, B, H, Nq, Nk, d, causal):
+    assert (Nq + 255) // 256 * B * H >= 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    Q, K, V = inputs.make_qkv(B, H, Nq, Nk, d, seed=Nq + 3 * Nk + d)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    O, L = gpu_forward(dev, Q, K, V, causal, scale)
+    rng = np.random.default_rng(Nq)
+    rows = np.unique(np.concatenate([np.arange(0, B * H * Nq, Nq), np.arange(Nq - 1, B * H * Nq, Nq),
+                                     rng.integers(0, B * H * Nq, 400)]))
+    Or, Lr = oracle.attention_rows(*bits(Q, K, V), causal, scale, rows)
+    idx = torch.as_tensor(rows, device=dev)
+    assert_close(O.reshape(-1, d)[idx], L.reshape(-1)[idx], Or, Lr, f"two-sub-tile grid {(B, H, Nq, Nk, d, causal)}")
