@@ -160,6 +160,19 @@ int subtiles_per_cta(const Problem& pr, int splits) {
   return ctas2 < 2LL * sm_count() ? 1 : 2;
 }
 
+// Items (b*H + h, key range) per scheduling group: as many as have their
+// K and V tiles fit in kL2GroupBytes together (at least one).
+constexpr long long kL2GroupBytes = 64LL << 20;
+
+int item_group(const Problem& pr, int splits) {
+  const long long items = pr.BH * splits;
+  const long long kv_bytes = 2LL * ((pr.Nk + splits - 1) / splits) * pr.d * 2;
+  long long g = kL2GroupBytes / (kv_bytes > 0 ? kv_bytes : 1);
+  if (g < 1) g = 1;
+  if (g > items) g = items;
+  return static_cast<int>(g);
+}
+
 // Launch of the tensor-core kernel over `splits` key ranges of `tiles_per_split`
 // tiles each (splits == 1: the whole key range, outputs O and LSE directly).
 int launch_forward(const void* Q, const void* K, const void* V, float* O, float* LSE,
@@ -191,6 +204,7 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   p.O_part = O_part;
   p.LSE_part = LSE_part;
   p.o_half = o_half ? 1 : 0;
+  p.item_group = item_group(pr, splits);
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
     return FA2_ERR_LAUNCH;
 

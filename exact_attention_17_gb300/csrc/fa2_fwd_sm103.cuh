@@ -76,6 +76,10 @@ struct FwdParams {
   float* LSE_part;
   // O in the input element type (16 bits) instead of fp32 (num_splits == 1).
   int o_half;
+  // Work items (b*H + h, key range) are scheduled in groups of item_group:
+  // within a group CTAs run query block by query block across the group's
+  // items, heaviest causal blocks first.
+  int item_group;
 };
 
 constexpr int kRowsPerSub = 128;   // tcgen05 M
@@ -174,15 +178,25 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: (pair u of query sub-tiles, key range, b*H + h).  Pairs of one
-  // head and range are adjacent so that concurrently running CTAs share K/V
-  // tiles through L2; under the causal mask the heaviest pairs start first.
+  // Work item: (query block u, key range, b*H + h).  Blocks are numbered
+  // group by group, a group being item_group consecutive (b*H + h, range)
+  // items chosen so that their K/V tiles fit in L2 together: concurrently
+  // running CTAs then share K/V through L2.  Within a group the numbering
+  // runs over the items for one query block before moving to the next, and
+  // under the causal mask the heaviest (last) query blocks come first, so the
+  // short CTAs fill the tail of the grid.
   const int U = p.q_blocks;
-  const int item = blockIdx.x / U;
+  const int items = p.BH * p.num_splits;
+  const int per_group = p.item_group * U;
+  const int group = blockIdx.x / per_group;
+  const int in_group = blockIdx.x - group * per_group;
+  const int g0 = group * p.item_group;
+  const int g_items = min(p.item_group, items - g0);
+  const int u_rank = in_group / g_items;
+  const int item = g0 + (in_group - u_rank * g_items);
   const int bh = item / p.num_splits;
   const int split = item - bh * p.num_splits;
-  int u = blockIdx.x - item * U;
-  if (CAUSAL) u = U - 1 - u;
+  const int u = CAUSAL ? U - 1 - u_rank : u_rank;
   const int all_tiles = (p.Nk + kKeysPerTile - 1) / kKeysPerTile;
   const int t_begin = split * p.tiles_per_split;
   const int t_end = min(all_tiles, t_begin + p.tiles_per_split);
