@@ -316,18 +316,29 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
           const int iv = 2 * j + 1, ik = 2 * j + 2;
           const int slot_v = iv % STAGES, slot_k = ik % STAGES;
           const bool next = j + 1 < nmax;
-          if (!wait_bar(&bars->kv_full[slot_v], (iv / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
+          // V_j, P_0(j) and K_(j+1) in one wait (a phase not needed is
+          // replaced by a repeat of V_j's): every pause of this thread idles
+          // the tensor pipe, and the three checks overlap.  With a two-slot
+          // ring K_(j+1) has only just been requested, so it is waited for
+          // after PV_0(j) instead.
+          constexpr bool kEarlyK = STAGES >= 4;
+          uint64_t* bv = &bars->kv_full[slot_v];
+          const uint32_t pv = (iv / STAGES) & 1;
+          uint64_t* bp = j < n0 ? &bars->p_ready[0] : bv;
+          const uint32_t pp = j < n0 ? (j & 1) : pv;
+          uint64_t* bk = kEarlyK && next ? &bars->kv_full[slot_k] : bv;
+          const uint32_t pk = kEarlyK && next ? (ik / STAGES) & 1 : pv;
+          if (!wait_bar3(bv, pv, bp, pp, bk, pk, abort, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after_sync();
           if (j < n0) {
-            if (!wait_bar(&bars->p_ready[0], j & 1, abort, p.timeout_ns)) { ok = false; break; }
-            tc_fence_after_sync();
             issue_pv(0, slot_v, j > 0);
             mma_commit(&bars->o_done[0]);
           }
-          if (next) {
+          if (!kEarlyK && next) {
             if (!wait_bar(&bars->kv_full[slot_k], (ik / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
             tc_fence_after_sync();
-            if (j + 1 < n0) { issue_s(0, slot_k); mma_commit(&bars->s_full[0]); }
           }
+          if (next && j + 1 < n0) { issue_s(0, slot_k); mma_commit(&bars->s_full[0]); }
           if (j < n1) {
             if (!wait_bar(&bars->p_ready[1], j & 1, abort, p.timeout_ns)) { ok = false; break; }
             tc_fence_after_sync();

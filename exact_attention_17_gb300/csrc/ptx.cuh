@@ -75,6 +75,35 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+// Three try_waits issued back to back, so that their latencies overlap;
+// true when all three phases have completed.
+__device__ __forceinline__ bool bar_try_wait3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
+                                              uint32_t b2, uint32_t p2) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "and.pred q0, q0, q1;\n\t"
+      "and.pred q0, q0, q2;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t}"
+      : "=r"(ok)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for three barrier phases (a barrier may be repeated).  Same bounds
+// and result as wait_bar.
+__device__ __forceinline__ bool wait_bar3(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
+                                          uint64_t* b2, uint32_t p2, volatile int* abort,
+                                          uint64_t timeout_ns) {
+  if (bar_try_wait3(smem_addr(b0), p0, smem_addr(b1), p1, smem_addr(b2), p2)) return true;
+  return wait_bar(b0, p0, abort, timeout_ns) && wait_bar(b1, p1, abort, timeout_ns) &&
+         wait_bar(b2, p2, abort, timeout_ns);
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {

@@ -194,17 +194,20 @@ class Sim:
         for j in range(nmax):
             gv, gk = 2 * j + 1, 2 * j + 2
             nxt = j + 1 < nmax
-            while not self.slot_full[gv % S].done(gv // S):
+            # one combined wait for V_j, P_0(j) and (ring of four or more
+            # slots) K_(j+1); with fewer slots K_(j+1) is waited for after PV_0(j)
+            early_k = S >= 4
+            while not (self.slot_full[gv % S].done(gv // S)
+                       and (j >= n0 or self.p_ready[0].done(j))
+                       and (not (early_k and nxt) or self.slot_full[gk % S].done(gk // S))):
                 yield
             if j < n0:
-                while not self.p_ready[0].done(j):
-                    yield
                 issue_pv(0, gv)
-            if nxt:
+            if not early_k and nxt:
                 while not self.slot_full[gk % S].done(gk // S):
                     yield
-                if j + 1 < n0:
-                    issue_s(0, gk)
+            if nxt and j + 1 < n0:
+                issue_s(0, gk)
             if j < n1:
                 while not self.p_ready[1].done(j):
                     yield
@@ -274,7 +277,7 @@ class Sim:
 
 
 CASES = []
-for stages in (4, 8):
+for stages in (2, 4, 5, 8):
     for nmax in list(range(1, 11)) + [17]:
         CASES.append((stages, nmax, nmax))          # non-causal: both sub-tiles, same range
         CASES.append((stages, nmax - 1, nmax) if nmax > 1 else (stages, 1, 1))  # causal pair
