@@ -10,6 +10,10 @@ FlashAttention-2 follow-up); this module compiles it with gcc and marshals
 numpy arrays through ctypes.  ``merge`` (the same page's ring-attention
 merge of partial results) is written here in numpy float64.
 
+``attention_backward`` gives the gradients of the same definition with
+respect to Q, K and V (the chain rule written out in ``attn_ref.c``; the
+pages name the backward pass but print no formulas).
+
 Parity pins (checked by the CPU test suite): the pages' worked online-softmax
 example, an independent library routine (torch's float64 CPU attention) on
 tiny shapes, closed forms (uniform weights when K = 0, a single kept key,
@@ -68,6 +72,12 @@ class Oracle:
                                                         ctypes.c_int]
             lib.oracle_widen.restype = ctypes.c_double
             lib.oracle_widen.argtypes = [ctypes.c_uint16, ctypes.c_int]
+        self.has_backward = hasattr(lib, "oracle_attention_backward")
+        if self.has_backward:
+            lib.oracle_attention_backward.restype = ctypes.c_int
+            lib.oracle_attention_backward.argtypes = [p, p, p, p, i64, i64, i64, i64, i64,
+                                                      ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                                      p, i64, p, p, p, p, p, p, ctypes.c_int]
         self.lib = lib
         self.path = lib_path
 
@@ -128,6 +138,35 @@ class Oracle:
         return O, LSE
 
 
+    def attention_backward(self, Q, K, V, dO, causal: bool, scale: float, heads=None,
+                           nthreads: int | None = None, dtype: str = "bf16",
+                           magnitudes: bool = False):
+        """Gradients of the attention definition for upstream gradient dO.
+
+        Q, dO [B,H,Nq,d] and K, V [B,H,Nk,d] are 16-bit patterns of `dtype`.
+        ``heads`` lists flattened head ids b*H + h (default: all, in order).
+        Returns (dQ [n,Nq,d], dK [n,Nk,d], dV [n,Nk,d]) float64 for the n heads,
+        followed by (M_dQ, M_dK, M_dV), the per-element sums of absolute
+        terms, when ``magnitudes`` is true.
+        """
+        Q, K, V, dO = _bits(Q), _bits(K), _bits(V), _bits(dO)
+        B, H, Nq, d = Q.shape
+        Nk = K.shape[2]
+        if K.shape != (B, H, Nk, d) or V.shape != K.shape or dO.shape != Q.shape:
+            raise ValueError("shape mismatch")
+        hl = np.arange(B * H, dtype=np.int64) if heads is None else np.ascontiguousarray(heads, dtype=np.int64)
+        n = hl.shape[0]
+        out = [np.empty((n, N, d), dtype=np.float64) for N in (Nq, Nk, Nk)]
+        mags = [np.empty((n, N, d), dtype=np.float64) for N in (Nq, Nk, Nk)] if magnitudes else None
+        mp = [_ptr(a) for a in mags] if magnitudes else [None, None, None]
+        rc = self.lib.oracle_attention_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, H, Nq, Nk, d,
+                                                int(bool(causal)), float(scale), _DTYPES[dtype],
+                                                _ptr(hl), n, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                                mp[0], mp[1], mp[2], nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_attention_backward failed with code {rc}")
+        return tuple(out) + (tuple(mags) if magnitudes else ())
+
     def widen(self, bits: int, dtype: str) -> float:
         """The oracle's exact widening of one 16-bit pattern to double."""
         return self.lib.oracle_widen(bits, _DTYPES[dtype])
@@ -175,6 +214,13 @@ def attention_rows(Q, K, V, causal: bool, scale: float, rows, nthreads: int | No
                    dtype: str = "bf16"):
     """Exact attention of selected rows (see ``Oracle.attention_rows``)."""
     return _default().attention_rows(Q, K, V, causal, scale, rows, nthreads, dtype)
+
+
+def attention_backward(Q, K, V, dO, causal: bool, scale: float, heads=None,
+                       nthreads: int | None = None, dtype: str = "bf16", magnitudes: bool = False):
+    """Gradients of the attention definition (see ``Oracle.attention_backward``)."""
+    return _default().attention_backward(Q, K, V, dO, causal, scale, heads, nthreads, dtype,
+                                         magnitudes)
 
 
 def widen(bits: int, dtype: str) -> float:

@@ -30,6 +30,9 @@
  *
  * Layout: Q [B,H,Nq,d], K and V [B,H,Nk,d], all contiguous (BHSD).  Outputs
  * are double: O [rows, d] and LSE [rows].
+ *
+ * oracle_attention_backward (below) gives the gradients of the same
+ * definition with respect to Q, K and V.
  */
 #include <math.h>
 #include <pthread.h>
@@ -221,6 +224,235 @@ int oracle_attention_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *
 double oracle_widen(uint16_t bits, int dtype)
 {
     return widen(bits, dtype);
+}
+
+/*
+ * Gradients of the attention above (the backward pass).  The pages name a
+ * backward pass that recomputes the scores from the saved logsumexp
+ * ("FlashAttention 怎么做?", FlashAttention-2 question; "Triton内核实战",
+ * closing section) but print no formulas, so this is the chain rule of the
+ * definition, written out for an upstream gradient dO:
+ *   s_ij  = scale q_i . k_j            (j in J_i)
+ *   p_ij  = exp(s_ij - LSE_i)          (the softmax weights)
+ *   dV_j  = sum over rows i with j in J_i of p_ij dO_i
+ *   dp_ij = dO_i . v_j
+ *   D_i   = sum_{j in J_i} p_ij dp_ij  (softmax Jacobian: the row term)
+ *   ds_ij = p_ij (dp_ij - D_i)
+ *   dQ_i  = scale sum_{j in J_i} ds_ij k_j
+ *   dK_j  = scale sum over rows i with j in J_i of ds_ij q_i
+ * Alongside each output element it returns the sum of the absolute values of
+ * the terms that element adds up (M_dQ = scale sum |ds_ij| |k_jc|, M_dK =
+ * scale sum |ds_ij| |q_ic|, M_dV = sum p_ij |dO_ic|): rounding one factor of
+ * every term to a b-bit significand changes the element by at most
+ * 2^-b times that sum.
+ */
+typedef struct {
+    const uint16_t *Q, *K, *V, *dO;
+    int64_t Nq, Nk, d;
+    int causal, dtype;
+    double scale;
+    int64_t bh;                 /* head being processed */
+    double *LSE, *Dr;           /* per query row of the head (phase 1 output) */
+    double *dQ, *dK, *dV, *MdQ, *MdK, *MdV;   /* this head's slices */
+    int64_t next, count;
+    int phase, error;
+} oracle_bwd_job;
+
+static int64_t kept_keys(const oracle_bwd_job *J, int64_t i)
+{
+    return (J->causal && i + 1 < J->Nk) ? i + 1 : J->Nk;
+}
+
+/* Phase 1, query row i: LSE_i, D_i and dQ_i. */
+static void bwd_query_row(oracle_bwd_job *J, int64_t i, double *s, double *dp)
+{
+    const int64_t d = J->d;
+    const uint16_t *q = J->Q + (J->bh * J->Nq + i) * d;
+    const uint16_t *g = J->dO + (J->bh * J->Nq + i) * d;
+    const uint16_t *kb = J->K + J->bh * J->Nk * d;
+    const uint16_t *vb = J->V + J->bh * J->Nk * d;
+    const int64_t n = kept_keys(J, i);
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        double acc = 0.0, gv = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            acc += widen(q[c], J->dtype) * widen(kb[j * d + c], J->dtype);
+            gv += widen(g[c], J->dtype) * widen(vb[j * d + c], J->dtype);
+        }
+        s[j] = J->scale * acc;
+        dp[j] = gv;
+        if (s[j] > m)
+            m = s[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j)
+        l += exp(s[j] - m);
+    const double lse = m + log(l);
+    double D = 0.0;
+    for (int64_t j = 0; j < n; ++j)
+        D += exp(s[j] - lse) * dp[j];
+    J->LSE[i] = lse;
+    J->Dr[i] = D;
+    double *dq = J->dQ + i * d, *mq = J->MdQ ? J->MdQ + i * d : NULL;
+    for (int64_t c = 0; c < d; ++c) {
+        dq[c] = 0.0;
+        if (mq)
+            mq[c] = 0.0;
+    }
+    for (int64_t j = 0; j < n; ++j) {
+        const double ds = exp(s[j] - lse) * (dp[j] - D);
+        for (int64_t c = 0; c < d; ++c) {
+            const double kc = widen(kb[j * d + c], J->dtype);
+            dq[c] += J->scale * ds * kc;
+            if (mq)
+                mq[c] += J->scale * fabs(ds) * fabs(kc);
+        }
+    }
+}
+
+/* Phase 2, key row j: dK_j and dV_j over the rows that keep key j. */
+static void bwd_key_row(oracle_bwd_job *J, int64_t j)
+{
+    const int64_t d = J->d;
+    const uint16_t *k = J->K + (J->bh * J->Nk + j) * d;
+    const uint16_t *v = J->V + (J->bh * J->Nk + j) * d;
+    const uint16_t *qb = J->Q + J->bh * J->Nq * d;
+    const uint16_t *gb = J->dO + J->bh * J->Nq * d;
+    double *dk = J->dK + j * d, *dv = J->dV + j * d;
+    double *mk = J->MdK ? J->MdK + j * d : NULL, *mv = J->MdV ? J->MdV + j * d : NULL;
+    for (int64_t c = 0; c < d; ++c) {
+        dk[c] = dv[c] = 0.0;
+        if (mk)
+            mk[c] = mv[c] = 0.0;
+    }
+    for (int64_t i = 0; i < J->Nq; ++i) {
+        if (j >= kept_keys(J, i))
+            continue;
+        double acc = 0.0, gv = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            acc += widen(qb[i * d + c], J->dtype) * widen(k[c], J->dtype);
+            gv += widen(gb[i * d + c], J->dtype) * widen(v[c], J->dtype);
+        }
+        const double p = exp(J->scale * acc - J->LSE[i]);
+        const double ds = p * (gv - J->Dr[i]);
+        for (int64_t c = 0; c < d; ++c) {
+            const double qc = widen(qb[i * d + c], J->dtype);
+            const double gc = widen(gb[i * d + c], J->dtype);
+            dv[c] += p * gc;
+            dk[c] += J->scale * ds * qc;
+            if (mk) {
+                mv[c] += p * fabs(gc);
+                mk[c] += J->scale * fabs(ds) * fabs(qc);
+            }
+        }
+    }
+}
+
+static void *oracle_bwd_worker(void *arg)
+{
+    oracle_bwd_job *J = (oracle_bwd_job *)arg;
+    const int64_t len = (J->Nk > J->Nq ? J->Nk : J->Nq) + 1;
+    double *s = (double *)malloc((size_t)len * sizeof(double));
+    double *dp = (double *)malloc((size_t)len * sizeof(double));
+    if (!s || !dp) {
+        __atomic_store_n(&J->error, 1, __ATOMIC_RELAXED);
+        free(s);
+        free(dp);
+        return NULL;
+    }
+    for (;;) {
+        int64_t r = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+        if (r >= J->count)
+            break;
+        if (J->phase == 1)
+            bwd_query_row(J, r, s, dp);
+        else
+            bwd_key_row(J, r);
+    }
+    free(s);
+    free(dp);
+    return NULL;
+}
+
+static int run_bwd_phase(oracle_bwd_job *J, int phase, int64_t count, int nthreads)
+{
+    J->phase = phase;
+    J->count = count;
+    J->next = 0;
+    pthread_t tid[1024];
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tid[started], NULL, oracle_bwd_worker, J) != 0)
+            break;
+        ++started;
+    }
+    oracle_bwd_worker(J);
+    for (int t = 0; t < started; ++t)
+        pthread_join(tid[t], NULL);
+    return J->error;
+}
+
+/*
+ * Gradients for selected heads.
+ *   Q [B,H,Nq,d], K and V [B,H,Nk,d], dO [B,H,Nq,d]: 16-bit patterns of `dtype`;
+ *   heads   flattened head ids b*H + h (NULL: every head in order), nheads of them;
+ *   dQ      nheads*Nq*d doubles, dK and dV nheads*Nk*d doubles (head-list order);
+ *   MdQ, MdK, MdV  the matching absolute-term sums, or all three NULL.
+ * Returns 0 on success, 1 on a bad argument, 2 if memory ran out.
+ */
+int oracle_attention_backward(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                              const uint16_t *dO, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                              int64_t d, int causal, float scale, int dtype, const int64_t *heads,
+                              int64_t nheads, double *dQ, double *dK, double *dV, double *MdQ,
+                              double *MdK, double *MdV, int nthreads)
+{
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV || B < 0 || H < 0 || Nq < 0 || Nk < 1 ||
+        d < 1 || nheads < 0)
+        return 1;
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16)
+        return 1;
+    if (!((MdQ && MdK && MdV) || (!MdQ && !MdK && !MdV)))
+        return 1;
+    if (!heads && nheads != B * H)
+        return 1;
+    if (heads)
+        for (int64_t t = 0; t < nheads; ++t)
+            if (heads[t] < 0 || heads[t] >= B * H)
+                return 1;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 1024)
+        nthreads = 1024;
+    double *lse = (double *)malloc((size_t)(Nq > 0 ? Nq : 1) * sizeof(double));
+    double *dr = (double *)malloc((size_t)(Nq > 0 ? Nq : 1) * sizeof(double));
+    if (!lse || !dr) {
+        free(lse);
+        free(dr);
+        return 2;
+    }
+    oracle_bwd_job J;
+    J.Q = Q; J.K = K; J.V = V; J.dO = dO;
+    J.Nq = Nq; J.Nk = Nk; J.d = d;
+    J.causal = causal ? 1 : 0;
+    J.dtype = dtype;
+    J.scale = (double)scale;
+    J.LSE = lse; J.Dr = dr;
+    J.error = 0;
+    int rc = 0;
+    for (int64_t t = 0; t < nheads && rc == 0; ++t) {
+        J.bh = heads ? heads[t] : t;
+        J.dQ = dQ + t * Nq * d;
+        J.dK = dK + t * Nk * d;
+        J.dV = dV + t * Nk * d;
+        J.MdQ = MdQ ? MdQ + t * Nq * d : NULL;
+        J.MdK = MdK ? MdK + t * Nk * d : NULL;
+        J.MdV = MdV ? MdV + t * Nk * d : NULL;
+        if (run_bwd_phase(&J, 1, Nq, nthreads) || run_bwd_phase(&J, 2, Nk, nthreads))
+            rc = 2;
+    }
+    free(lse);
+    free(dr);
+    return rc;
 }
 
 /* Every row of every (b, h): O [B,H,Nq,d], LSE [B,H,Nq]. */
