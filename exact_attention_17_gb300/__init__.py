@@ -42,6 +42,8 @@ SIGNATURES = {
     "fa2_forward_splitkv": (_I, _FORWARD_ARGS[:-1] + [_I, _P, _Z, _P]),
     "fa2_merge": (_I, [_P, _P, _I, _LL, _I, _P, _P, _P]),
     "fa2_forward_splitkv_static": (_I, _FORWARD_ARGS[:-1] + [_I, _P]),
+    "fa2_backward_workspace_bytes": (_Z, [_I, _I, _I]),
+    "fa2_backward": (_I, [_P] * 9 + [_I] * 6 + [ctypes.c_float, _P, _Z, _P]),
     "fa2_status_string": (ctypes.c_char_p, [_I]),
     "fa2_device_status": (_I, [_P, _I]),
 }
@@ -110,6 +112,17 @@ def fa2_forward_splitkv_static(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, 
 def fa2_merge(O_parts, LSE_parts, num_parts, rows, d, O, LSE, stream) -> int:
     """Raw C call of the merge of partial attention results."""
     return library().fa2_merge(O_parts, LSE_parts, num_parts, rows, d, O, LSE, stream)
+
+
+def fa2_backward_workspace_bytes(B, H, Nq) -> int:
+    return library().fa2_backward_workspace_bytes(B, H, Nq)
+
+
+def fa2_backward(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, workspace,
+                 workspace_size, stream) -> int:
+    """Raw C call of the backward pass (caller-provided device workspace)."""
+    return library().fa2_backward(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d,
+                                  int(bool(causal)), scale, workspace, workspace_size, stream)
 
 
 def fa2_status_string(status: int) -> str:
@@ -218,3 +231,47 @@ def merge(o_parts, lse_parts, out=None, lse=None, stream=None):
     if rc != FA2_OK:
         raise FA2Error(rc, "fa2_merge")
     return out, lse
+
+
+def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, dq=None,
+             dk=None, dv=None, workspace=None, stream=None):
+    """Attention backward on torch CUDA tensors (fa2_backward).
+
+    q, do: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; o fp32 [B,H,Nq,d] and lse
+    fp32 [B,H,Nq] as returned by ``forward`` for the same inputs.  Returns
+    fp32 (dQ, dK, dV).  The workspace (a uint8 CUDA tensor) is allocated here
+    unless given.
+    """
+    import torch
+
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("do", do, torch.bfloat16), ("o", o, torch.float32), ("lse", lse, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if (tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d)
+            or tuple(o.shape) != (B, H, Nq, d) or tuple(do.shape) != (B, H, Nq, d)
+            or tuple(lse.shape) != (B, H, Nq)):
+        raise ValueError("shapes must be q, o, do [B,H,Nq,d], k, v [B,H,Nk,d], lse [B,H,Nq]")
+    if scale is None:
+        scale = float(torch.tensor(d, dtype=torch.float64).rsqrt().float())
+    outs = []
+    for name, t, shape in (("dq", dq, (B, H, Nq, d)), ("dk", dk, (B, H, Nk, d)), ("dv", dv, (B, H, Nk, d))):
+        if t is None:
+            t = torch.empty(shape, dtype=torch.float32, device=q.device)
+        if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous fp32 tensor of shape {shape} on {q.device}")
+        outs.append(t)
+    dq, dk, dv = outs
+    need = fa2_backward_workspace_bytes(B, H, Nq)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = fa2_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
+                          causal, float(scale), workspace.data_ptr(), workspace.numel(),
+                          _stream_handle(stream))
+    if rc != FA2_OK:
+        raise FA2Error(rc, "fa2_backward")
+    return dq, dk, dv

@@ -68,7 +68,7 @@ int device_ready() {
     if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return;
     if (fa2host::prepare_tc_d64_bf16() != cudaSuccess || fa2host::prepare_tc_d128_bf16() != cudaSuccess ||
         fa2host::prepare_tc_d64_f16() != cudaSuccess || fa2host::prepare_tc_d128_f16() != cudaSuccess ||
-        fa2host::prepare_simt() != cudaSuccess)
+        fa2host::prepare_simt() != cudaSuccess || fa2host::prepare_bwd() != cudaSuccess)
       return;
     st.usable = true;
   });
@@ -239,6 +239,12 @@ size_t workspace_bytes(long long BH, int Nq, int d, int splits) {
   return align256(static_cast<size_t>(splits) * rows * d * 4) + align256(static_cast<size_t>(splits) * rows * 4);
 }
 
+// Backward workspace: LSE log2(e), then D, each [BH][Nq rounded up to 128] fp32.
+size_t bwd_workspace_bytes(long long BH, int Nq) {
+  const size_t pad = (static_cast<size_t>(Nq) + 127) / 128 * 128;
+  return 2 * align256(static_cast<size_t>(BH) * pad * 4);
+}
+
 }  // namespace
 
 extern "C" int fa2_forward(const void* Q, const void* K, const void* V, float* O, float* LSE, int B,
@@ -341,6 +347,94 @@ extern "C" int fa2_forward_simt(const void* Q, const void* K, const void* V, flo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = fa2host::launch_simt(d, causal != 0, p, grid, s);
   return e == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
+}
+
+extern "C" size_t fa2_backward_workspace_bytes(int B, int H, int Nq) {
+  if (B < 0 || H < 0 || Nq < 0) return 0;
+  return bwd_workspace_bytes(static_cast<long long>(B) * H, Nq);
+}
+
+extern "C" int fa2_backward(const void* Q, const void* K, const void* V, const float* O,
+                            const void* dO, const float* LSE, float* dQ, float* dK, float* dV,
+                            int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                            void* workspace, size_t workspace_size, fa2_stream_t stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA2_ERR_SHAPE;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH == 0 || (Nq == 0 && Nk == 0)) return FA2_OK;
+  if (BH > 0x7fffffffLL) return FA2_ERR_SHAPE;
+  if (Nq > 0 && Nk == 0) return FA2_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA2_ERR_HEADDIM;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA2_ERR_SCALE;
+  if (!dK || !dV) return FA2_ERR_NULL;
+  if (Nq > 0 && (!Q || !K || !V || !O || !dO || !LSE || !dQ || !workspace)) return FA2_ERR_NULL;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                        reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
+                        reinterpret_cast<uintptr_t>(dO) | reinterpret_cast<uintptr_t>(dQ) |
+                        reinterpret_cast<uintptr_t>(dK) | reinterpret_cast<uintptr_t>(dV);
+  if ((a16 & 15u) != 0 || (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FA2_ERR_ALIGN;
+  int rc = device_ready();
+  if (rc != FA2_OK) return rc;
+  const size_t bh = static_cast<size_t>(BH);
+  const size_t q_elems = bh * Nq * d, kv_elems = bh * Nk * d;
+  if (!device_range_ok(dK, kv_elems * 4) || !device_range_ok(dV, kv_elems * 4)) return FA2_ERR_MEMORY;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (Nq == 0) {
+    // no query sees any key: the gradients of K and V are zero
+    if (fa2host::launch_zero(dK, static_cast<long long>(kv_elems), s) != cudaSuccess ||
+        fa2host::launch_zero(dV, static_cast<long long>(kv_elems), s) != cudaSuccess)
+      return FA2_ERR_LAUNCH;
+    return FA2_OK;
+  }
+  const size_t need = bwd_workspace_bytes(BH, Nq);
+  if (!device_range_ok(Q, q_elems * 2) || !device_range_ok(K, kv_elems * 2) ||
+      !device_range_ok(V, kv_elems * 2) || !device_range_ok(O, q_elems * 4) ||
+      !device_range_ok(dO, q_elems * 2) || !device_range_ok(LSE, bh * Nq * 4) ||
+      !device_range_ok(dQ, q_elems * 4) || workspace_size < need ||
+      !device_range_ok(workspace, need))
+    return FA2_ERR_MEMORY;
+
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_map(&mq, Q, d, Nq, static_cast<int>(BH), false) ||
+      !encode_map(&mk, K, d, Nk, static_cast<int>(BH), false) ||
+      !encode_map(&mv, V, d, Nk, static_cast<int>(BH), false) ||
+      !encode_map(&mdo, dO, d, Nq, static_cast<int>(BH), false))
+    return FA2_ERR_SHAPE;
+
+  const int Nq_pad = (Nq + 127) / 128 * 128;
+  float* L2 = static_cast<float*>(workspace);
+  float* Dr = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(bh * Nq_pad * 4));
+  if (fa2host::launch_bwd_pre(d, O, dO, LSE, dQ, L2, Dr, static_cast<long long>(bh) * Nq, Nq, Nq_pad,
+                              s) != cudaSuccess)
+    return FA2_ERR_LAUNCH;
+
+  fa2dev::BwdParams p;
+  p.dQ = dQ;
+  p.dK = dK;
+  p.dV = dV;
+  p.L2 = L2;
+  p.Dr = Dr;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.Nq_pad = Nq_pad;
+  p.BH = static_cast<int>(BH);
+  p.key_blocks = key_tiles(Nk);
+  // heads per scheduling group: their Q and dO tiles fit in kL2GroupBytes together
+  const long long qd_bytes = 2LL * Nq * d * 2;
+  long long g = kL2GroupBytes / (qd_bytes > 0 ? qd_bytes : 1);
+  p.item_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.timeout_ns = kWaitTimeoutNs;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
+    return FA2_ERR_LAUNCH;
+  const long long grid = BH * p.key_blocks;
+  if (grid > 0x7fffffffLL) return FA2_ERR_SHAPE;
+  return fa2host::launch_bwd(d, causal != 0, mq, mk, mv, mdo, p, static_cast<unsigned>(grid), s) ==
+                 cudaSuccess
+             ? FA2_OK
+             : FA2_ERR_LAUNCH;
 }
 
 extern "C" const char* fa2_status_string(int status) {

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa2_bwd_sm103.cuh"
 #include "fa2_fwd_simt.cuh"
 #include "fa2_fwd_sm103.cuh"
 
@@ -32,5 +33,15 @@ cudaError_t launch_simt(int d, bool causal, const fa2dev::SimtParams& p, dim3 gr
 // Merge of S partial results (normalised O [S, R, d], LSE [S, R]) into O [R, d], LSE [R].
 cudaError_t launch_combine(int d, const float* O_part, const float* LSE_part, int S, long long R,
                            float* O, float* LSE, cudaStream_t s);
+
+// Backward pass (fa2_bwd.cu).
+cudaError_t prepare_bwd();
+cudaError_t launch_bwd(int d, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
+                       const CUtensorMap& mv, const CUtensorMap& mdo, const fa2dev::BwdParams& p,
+                       unsigned grid, cudaStream_t s);
+// D_i = dO_i . O_i and LSE_i log2(e) into [BH][Nq_pad] arrays; dQ rows zeroed.
+cudaError_t launch_bwd_pre(int d, const float* O, const void* dO, const float* LSE, float* dQ,
+                           float* L2, float* Dr, long long rows, int Nq, int Nq_pad, cudaStream_t s);
+cudaError_t launch_zero(float* p, long long n, cudaStream_t s);
 
 }  // namespace fa2host

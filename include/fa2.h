@@ -1,6 +1,6 @@
 /*
- * fa2.h -- C ABI of libfa2.so, a FlashAttention-2 forward pass for GB300
- * (sm_103a).
+ * fa2.h -- C ABI of libfa2.so, the FlashAttention-2 forward pass (and its
+ * backward pass) for GB300 (sm_103a).
  *
  * The operation (per batch b, head h and query row i):
  *
@@ -175,6 +175,45 @@ int fa2_merge(const float *O_parts, const float *LSE_parts, int num_parts, long 
 int fa2_forward_splitkv_static(const void *Q, const void *K, const void *V, float *O, float *LSE,
                                int B, int H, int Nq, int Nk, int d, int causal, float scale,
                                int num_splits, fa2_stream_t stream);
+
+/*
+ * Bytes of device workspace fa2_backward needs: 2 * (B*H * ceil(Nq/128)*128 *
+ * 4 bytes), each half rounded up to 256 bytes.  0 for negative sizes.
+ */
+size_t fa2_backward_workspace_bytes(int B, int H, int Nq);
+
+/*
+ * Backward pass: the gradients of the attention above with respect to Q, K
+ * and V for an upstream gradient dO.  The pages name this pass -- it reuses
+ * the forward pass's per-row logsumexp and recomputes the scores block by
+ * block ("FlashAttention 怎么做?", FlashAttention-2 question; "Triton内核实战",
+ * closing section) -- but print no formulas; it computes the chain rule of
+ * the definition:
+ *     p_ij  = exp(s_ij - LSE_i)            (j in J_i)
+ *     dV_j  = sum_i p_ij dO_i              dp_ij = dO_i . v_j
+ *     D_i   = dO_i . O_i                   ds_ij = p_ij (dp_ij - D_i)
+ *     dQ_i  = scale sum_j ds_ij k_j        dK_j  = scale sum_i ds_ij q_i
+ *   Q, K, V   device bf16 inputs of the forward pass (layouts above)
+ *   O, LSE    device fp32 outputs of fa2_forward for these inputs
+ *   dO        device bf16 [B, H, Nq, d], the upstream gradient
+ *   dQ        device fp32 [B, H, Nq, d]  } outputs, fully overwritten
+ *   dK, dV    device fp32 [B, H, Nk, d]  }
+ *   workspace device scratch of fa2_backward_workspace_bytes(B, H, Nq) bytes
+ *             or more, 256-byte aligned, owned by the caller; its contents
+ *             on entry do not matter
+ *   B, H, Nq, Nk, d, causal, scale, stream   as in fa2_forward
+ * Q, K, V, O, dO, dQ, dK and dV must be 16-byte aligned, LSE 4-byte aligned.
+ * B*H == 0 is a valid empty problem.  Nq == 0 with Nk > 0 writes zeros to dK
+ * and dV (no query sees any key); Q, K, V, O, dO, LSE, dQ and workspace may
+ * then be NULL.  Nk == 0 with Nq > 0 is FA2_ERR_SHAPE.  Keys that no query
+ * sees under the causal mask (j >= Nq) get zero gradients.  Errors as for
+ * fa2_forward; the other outputs are undefined after an error found on the
+ * device.
+ */
+int fa2_backward(const void *Q, const void *K, const void *V, const float *O, const void *dO,
+                 const float *LSE, float *dQ, float *dK, float *dV, int B, int H, int Nq, int Nk,
+                 int d, int causal, float scale, void *workspace, size_t workspace_size,
+                 fa2_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char *fa2_status_string(int status);

@@ -240,11 +240,16 @@ double oracle_widen(uint16_t bits, int dtype)
  *   ds_ij = p_ij (dp_ij - D_i)
  *   dQ_i  = scale sum_{j in J_i} ds_ij k_j
  *   dK_j  = scale sum over rows i with j in J_i of ds_ij q_i
- * Alongside each output element it returns the sum of the absolute values of
- * the terms that element adds up (M_dQ = scale sum |ds_ij| |k_jc|, M_dK =
- * scale sum |ds_ij| |q_ic|, M_dV = sum p_ij |dO_ic|): rounding one factor of
- * every term to a b-bit significand changes the element by at most
- * 2^-b times that sum.
+ * Alongside each output element it returns a magnitude from which rounding
+ * bounds for a low-precision implementation follow:
+ *   M_dV_jc = sum_i p_ij |dO_ic|
+ *   M_dQ_ic = scale sum_j (|ds_ij| + p_ij A_i) |k_jc|
+ *   M_dK_jc = scale sum_i (|ds_ij| + p_ij A_i) |q_ic|
+ * with A_i = sum_j p_ij sum_c |dO_ic| |v_jc|.  Rounding p (for dV) or ds
+ * (for dQ, dK) to a b-bit significand moves an element by at most 2^-b times
+ * the |p| or |ds| part; computing D_i from an output o_i whose weights were
+ * rounded that way moves D_i by at most 2^-b A_i, hence ds_ij by p_ij 2^-b
+ * A_i, which the p_ij A_i part covers.
  */
 typedef struct {
     const uint16_t *Q, *K, *V, *dO;
@@ -252,7 +257,7 @@ typedef struct {
     int causal, dtype;
     double scale;
     int64_t bh;                 /* head being processed */
-    double *LSE, *Dr;           /* per query row of the head (phase 1 output) */
+    double *LSE, *Dr, *Ar;      /* per query row of the head (phase 1 output) */
     double *dQ, *dK, *dV, *MdQ, *MdK, *MdV;   /* this head's slices */
     int64_t next, count;
     int phase, error;
@@ -264,7 +269,7 @@ static int64_t kept_keys(const oracle_bwd_job *J, int64_t i)
 }
 
 /* Phase 1, query row i: LSE_i, D_i and dQ_i. */
-static void bwd_query_row(oracle_bwd_job *J, int64_t i, double *s, double *dp)
+static void bwd_query_row(oracle_bwd_job *J, int64_t i, double *s, double *dp, double *da)
 {
     const int64_t d = J->d;
     const uint16_t *q = J->Q + (J->bh * J->Nq + i) * d;
@@ -274,13 +279,15 @@ static void bwd_query_row(oracle_bwd_job *J, int64_t i, double *s, double *dp)
     const int64_t n = kept_keys(J, i);
     double m = -INFINITY;
     for (int64_t j = 0; j < n; ++j) {
-        double acc = 0.0, gv = 0.0;
+        double acc = 0.0, gv = 0.0, ga = 0.0;
         for (int64_t c = 0; c < d; ++c) {
             acc += widen(q[c], J->dtype) * widen(kb[j * d + c], J->dtype);
             gv += widen(g[c], J->dtype) * widen(vb[j * d + c], J->dtype);
+            ga += fabs(widen(g[c], J->dtype)) * fabs(widen(vb[j * d + c], J->dtype));
         }
         s[j] = J->scale * acc;
         dp[j] = gv;
+        da[j] = ga;
         if (s[j] > m)
             m = s[j];
     }
@@ -288,11 +295,14 @@ static void bwd_query_row(oracle_bwd_job *J, int64_t i, double *s, double *dp)
     for (int64_t j = 0; j < n; ++j)
         l += exp(s[j] - m);
     const double lse = m + log(l);
-    double D = 0.0;
-    for (int64_t j = 0; j < n; ++j)
+    double D = 0.0, A = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
         D += exp(s[j] - lse) * dp[j];
+        A += exp(s[j] - lse) * da[j];
+    }
     J->LSE[i] = lse;
     J->Dr[i] = D;
+    J->Ar[i] = A;
     double *dq = J->dQ + i * d, *mq = J->MdQ ? J->MdQ + i * d : NULL;
     for (int64_t c = 0; c < d; ++c) {
         dq[c] = 0.0;
@@ -301,11 +311,12 @@ static void bwd_query_row(oracle_bwd_job *J, int64_t i, double *s, double *dp)
     }
     for (int64_t j = 0; j < n; ++j) {
         const double ds = exp(s[j] - lse) * (dp[j] - D);
+        const double w = fabs(ds) + exp(s[j] - lse) * A;
         for (int64_t c = 0; c < d; ++c) {
             const double kc = widen(kb[j * d + c], J->dtype);
             dq[c] += J->scale * ds * kc;
             if (mq)
-                mq[c] += J->scale * fabs(ds) * fabs(kc);
+                mq[c] += J->scale * w * fabs(kc);
         }
     }
 }
@@ -335,6 +346,7 @@ static void bwd_key_row(oracle_bwd_job *J, int64_t j)
         }
         const double p = exp(J->scale * acc - J->LSE[i]);
         const double ds = p * (gv - J->Dr[i]);
+        const double w = fabs(ds) + p * J->Ar[i];
         for (int64_t c = 0; c < d; ++c) {
             const double qc = widen(qb[i * d + c], J->dtype);
             const double gc = widen(gb[i * d + c], J->dtype);
@@ -342,7 +354,7 @@ static void bwd_key_row(oracle_bwd_job *J, int64_t j)
             dk[c] += J->scale * ds * qc;
             if (mk) {
                 mv[c] += p * fabs(gc);
-                mk[c] += J->scale * fabs(ds) * fabs(qc);
+                mk[c] += J->scale * w * fabs(qc);
             }
         }
     }
@@ -354,10 +366,12 @@ static void *oracle_bwd_worker(void *arg)
     const int64_t len = (J->Nk > J->Nq ? J->Nk : J->Nq) + 1;
     double *s = (double *)malloc((size_t)len * sizeof(double));
     double *dp = (double *)malloc((size_t)len * sizeof(double));
-    if (!s || !dp) {
+    double *da = (double *)malloc((size_t)len * sizeof(double));
+    if (!s || !dp || !da) {
         __atomic_store_n(&J->error, 1, __ATOMIC_RELAXED);
         free(s);
         free(dp);
+        free(da);
         return NULL;
     }
     for (;;) {
@@ -365,12 +379,13 @@ static void *oracle_bwd_worker(void *arg)
         if (r >= J->count)
             break;
         if (J->phase == 1)
-            bwd_query_row(J, r, s, dp);
+            bwd_query_row(J, r, s, dp, da);
         else
             bwd_key_row(J, r);
     }
     free(s);
     free(dp);
+    free(da);
     return NULL;
 }
 
@@ -425,9 +440,11 @@ int oracle_attention_backward(const uint16_t *Q, const uint16_t *K, const uint16
         nthreads = 1024;
     double *lse = (double *)malloc((size_t)(Nq > 0 ? Nq : 1) * sizeof(double));
     double *dr = (double *)malloc((size_t)(Nq > 0 ? Nq : 1) * sizeof(double));
-    if (!lse || !dr) {
+    double *ar = (double *)malloc((size_t)(Nq > 0 ? Nq : 1) * sizeof(double));
+    if (!lse || !dr || !ar) {
         free(lse);
         free(dr);
+        free(ar);
         return 2;
     }
     oracle_bwd_job J;
@@ -436,7 +453,7 @@ int oracle_attention_backward(const uint16_t *Q, const uint16_t *K, const uint16
     J.causal = causal ? 1 : 0;
     J.dtype = dtype;
     J.scale = (double)scale;
-    J.LSE = lse; J.Dr = dr;
+    J.LSE = lse; J.Dr = dr; J.Ar = ar;
     J.error = 0;
     int rc = 0;
     for (int64_t t = 0; t < nheads && rc == 0; ++t) {
@@ -452,6 +469,7 @@ int oracle_attention_backward(const uint16_t *Q, const uint16_t *K, const uint16
     }
     free(lse);
     free(dr);
+    free(ar);
     return rc;
 }
 

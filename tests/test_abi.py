@@ -91,3 +91,40 @@ def test_typed_entry_point_rejects_bad_element_types_on_the_host(lib):
     # valid types, empty problem: nothing launched
     empty = (16, 16, 16, 16, 16, 0, 1, 8, 8, 64, 0, 0.125)
     assert fa2.fa2_forward_typed(*empty, fa2.FA2_DTYPE_FP16, fa2.FA2_DTYPE_FP16, None) == fa2.FA2_OK
+
+
+def test_backward_workspace_bytes(lib):
+    # two [B*H][ceil(Nq/128)*128] fp32 arrays, each rounded up to 256 bytes
+    assert fa2.fa2_backward_workspace_bytes(1, 1, 1) == 2 * 512
+    assert fa2.fa2_backward_workspace_bytes(2, 3, 200) == 2 * 6 * 256 * 4
+    assert fa2.fa2_backward_workspace_bytes(1, 1, 0) == 0
+    assert fa2.fa2_backward_workspace_bytes(-1, 1, 8) == 0
+
+
+def test_backward_host_side_argument_errors(lib):
+    def c(**kw):
+        a = dict(Q=16, K=16, V=16, O=16, dO=16, LSE=16, dQ=16, dK=16, dV=16, B=1, H=1, Nq=8, Nk=8,
+                 d=64, causal=0, scale=0.125, ws=256, wss=1 << 20)
+        a.update(kw)
+        return fa2.fa2_backward(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["LSE"], a["dQ"], a["dK"],
+                                a["dV"], a["B"], a["H"], a["Nq"], a["Nk"], a["d"], a["causal"],
+                                a["scale"], a["ws"], a["wss"], None)
+
+    # empty problems launch nothing
+    assert c(B=0) == fa2.FA2_OK
+    assert c(Nq=0, Nk=0) == fa2.FA2_OK
+    # sizes
+    assert c(Nq=-1) == fa2.FA2_ERR_SHAPE
+    assert c(Nk=0) == fa2.FA2_ERR_SHAPE
+    for d in (0, 32, 96, 256):
+        assert c(d=d) == fa2.FA2_ERR_HEADDIM
+    for s in (0.0, -1.0, float("inf"), float("nan")):
+        assert c(scale=s) == fa2.FA2_ERR_SCALE
+    for name in ("Q", "K", "V", "O", "dO", "LSE", "dQ", "dK", "dV", "ws"):
+        assert c(**{name: None}) == fa2.FA2_ERR_NULL
+    # with no query rows only dK and dV are needed
+    assert c(Nq=0, dK=None) == fa2.FA2_ERR_NULL
+    for name in ("Q", "K", "V", "O", "dO", "dQ", "dK", "dV"):
+        assert c(**{name: 24}) == fa2.FA2_ERR_ALIGN
+    assert c(LSE=18) == fa2.FA2_ERR_ALIGN
+    assert c(ws=272) == fa2.FA2_ERR_ALIGN
