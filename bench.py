@@ -40,16 +40,20 @@ import torch  # noqa: E402
 from exact_attention_17_gb300 import inputs  # noqa: E402
 
 METRIC = "FA2 fwd TFLOP/s (causal-halved) and % of GB300 dense-BF16 tensor peak"
+METRIC_BWD = "FA2 bwd TFLOP/s (5 GEMMs = 2.5x fwd FLOPs, causal-halved) and % of GB300 dense-BF16 tensor peak"
 DEFAULT_WORKLOAD = "b1_h32_n16384_d128_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+BWD_KERNEL_SOURCES = ["exact_attention_17_gb300/csrc/fa2_bwd_sm103.cuh",
+                      "exact_attention_17_gb300/csrc/ptx.cuh",
+                      "exact_attention_17_gb300/csrc/fa2_bwd.cu"]
 KERNEL_SOURCES = ["exact_attention_17_gb300/csrc/fa2_fwd_sm103.cuh",
                   "exact_attention_17_gb300/csrc/ptx.cuh",
                   "exact_attention_17_gb300/csrc/fa2_tc_d128_bf16.cu"]
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -65,13 +69,20 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def algorithmic_bytes_backward(w) -> float:
+    """Q, K, V and dO read once as bf16, O (fp32) and LSE read once; dQ, dK and
+    dV written once as fp32."""
+    return w.B * w.H * (2.0 * w.Nq * w.d + 4.0 * w.Nk * w.d + 2.0 * w.Nq * w.d + 4.0 * w.Nq * w.d
+                        + 4.0 * w.Nq + 4.0 * w.Nq * w.d + 8.0 * w.Nk * w.d)
+
+
 def algorithmic_bytes(w, o_bytes: int = 4) -> float:
     """Q, K, V read once as 16-bit values; O written once (fp32 unless
     `o_bytes` says otherwise) and the fp32 LSE written once."""
     return w.B * w.H * (2.0 * w.Nq * w.d + 4.0 * w.Nk * w.d + o_bytes * w.Nq * w.d + 4.0 * w.Nq)
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, sources=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; otherwise None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -81,7 +92,7 @@ def recorded_traffic(workload: str):
     except (OSError, ValueError):
         return None
     entry = rec.get(workload)
-    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash(sources):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -195,11 +206,44 @@ def oracle_sample_rate(w, Q, K, V, budget_s: float, seed: int = 0):
     return flops / el / 1e12, cores, rows_done, el
 
 
+def backward_sample_shape(w, budget_s: float):
+    """The oracle's backward on one head costs about 9 d flops per kept (query,
+    key) pair and phase at roughly 4 Gflop/s per core: the largest leading
+    square of one head that fits the budget (the whole head when it does)."""
+    rate = 4e9 * (os.cpu_count() or 1)
+    n = min(w.Nq, w.Nk)
+    while n > 128:
+        pairs = n * n / (2 if w.causal else 1)
+        if 2 * 9 * w.d * pairs / rate <= budget_s:
+            break
+        n //= 2
+    return n
+
+
+def oracle_backward_rate(w, Q, K, V, G, budget_s: float):
+    """Time the fp64 oracle's backward on one head (truncated to its leading
+    n x n block when the whole head would exceed the budget).  Returns
+    (TFLOP/s, cores, n, seconds) with the algorithmic 2.5x forward FLOPs of
+    the timed problem."""
+    import oracle
+
+    n = backward_sample_shape(w, budget_s)
+    qb, kb, vb, gb = (np.ascontiguousarray(inputs.bf16_bits(t)[:1, :1, :n]) for t in (Q, K, V, G))
+    cores = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.attention_backward(qb, kb, vb, gb, w.causal, w.scale, nthreads=cores)
+    el = time.perf_counter() - t0
+    flops = 2.5 * 4.0 * n * n * w.d / (2 if w.causal else 1)
+    return flops / el / 1e12, cores, n, el
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     Q, K, V = inputs.workload_inputs(w)
+    if args.pass_ == "backward":
+        return run_reference_backward(args, w, Q, K, V)
     per_step = []
     rows_total = 0
     cores = 0
@@ -229,6 +273,35 @@ def run_reference(args, w):
     return 0
 
 
+def run_reference_backward(args, w, Q, K, V):
+    G = inputs.draw_bf16((w.B, w.H, w.Nq, w.d), w.seed, 3)
+    per_step = []
+    cores, n = 0, 0
+    for s in range(args.warmup + args.steps):
+        budget = 1.0 if s < args.warmup else args.reference_step_s
+        tf, cores, n, el = oracle_backward_rate(w, Q, K, V, G, budget)
+        if s >= args.warmup:
+            per_step.append((tf, el))
+    secs = sum(e for _, e in per_step)
+    value = sum(tf * e for tf, e in per_step) / secs
+    sample = (f"head 0 of {w.name} truncated to its leading {n} queries and keys, once per step, "
+              f"fp64 oracle backward, FLOPs = 2.5 x the forward's")
+    line = {
+        "impl": "reference", "metric": METRIC_BWD, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1000 * secs / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": dict(workload_config(w, "oracle on host cores"), **{"pass": "backward"}),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def workload_config(w, l2_note):
     return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
             "causal": w.causal, "scale": w.scale, "qk_dist": f"{w.qk_dist}(std {w.qk_std})",
@@ -239,13 +312,13 @@ def workload_config(w, l2_note):
 # ---------------------------------------------------------------- GPU arm
 
 def roofline_entry(hbm_bound, achieved_tflops, peak_tflops, peak_src, peaks, traffic, flops,
-                   algo_bytes, mean_launch_ms):
+                   algo_bytes, mean_launch_ms, kernel="fa2dev::fa2_fwd_tc_kernel"):
     """The roofline object for the forward kernel: against the measured HBM
     copy bandwidth when the workload sits below the machine balance, else
     against the measured bf16 tensor throughput."""
     common = {
         "traffic": traffic,
-        "kernel": "fa2dev::fa2_fwd_tc_kernel",
+        "kernel": kernel,
         "flops_per_launch": flops,
         "algorithmic_bytes_per_launch": algo_bytes,
         "mean_launch_ms": round(mean_launch_ms, 4),
@@ -282,6 +355,8 @@ def main():
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count (smaller profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
+                    help="time the forward pass (default) or the backward pass")
     args = ap.parse_args()
     w = inputs.workload(args.workload)
     if args.heads is not None:
@@ -307,6 +382,9 @@ def main():
     torch.cuda.set_device(dev)
 
     import exact_attention_17_gb300 as fa2
+
+    if args.pass_ == "backward":
+        return run_backward(args, w, fa2, dev, dist, world, rank)
 
     # seeded inputs, generated on the host (same bits the oracle sees)
     in_dtype = torch.float16 if args.dtype == "fp16" else torch.bfloat16
@@ -450,6 +528,146 @@ def main():
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (2 if args.num_splits > 1 else 1),
         "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+
+def run_backward(args, w, fa2, dev, dist, world, rank):
+    """One step = one backward pass (pre-pass + tensor-core kernel) of the
+    workload, with O and LSE from one forward pass before the timed region."""
+    if args.dtype != "bf16" or args.num_splits != 1 or args.out_dtype != "fp32":
+        raise SystemExit("--pass backward takes bf16 inputs, fp32 O and no split")
+    Qh, Kh, Vh = inputs.make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.seed, w.qk_dist, w.qk_std, w.v_dist)
+    Gh = inputs.draw_bf16((w.B, w.H, w.Nq, w.d), w.seed, 3)
+    Q, K, V, G = (t.to(dev) for t in (Qh, Kh, Vh, Gh))
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        O, L = fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, stream=stream)
+        dQ = torch.empty(w.B, w.H, w.Nq, w.d, device=dev)
+        dK = torch.empty(w.B, w.H, w.Nk, w.d, device=dev)
+        dV = torch.empty(w.B, w.H, w.Nk, w.d, device=dev)
+        ws = torch.empty(max(fa2.fa2_backward_workspace_bytes(w.B, w.H, w.Nq), 1), dtype=torch.uint8,
+                         device=dev)
+    in_bytes = algorithmic_bytes_backward(w)
+    l2_bytes = 129 * 1024 * 1024
+    flush = None
+    if in_bytes <= 2 * l2_bytes:
+        flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+        l2_note = "L2 flushed between steps (256 MiB write, outside the kernel events)"
+    else:
+        l2_note = f"operands {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"
+
+    def step(s):
+        fa2.backward(Q, K, V, O, L, G, causal=w.causal, scale=w.scale, dq=dQ, dk=dK, dv=dV,
+                     workspace=ws, stream=s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(stream)
+    torch.cuda.synchronize(dev)
+    if fa2.fa2_device_status(None, reset=True) != fa2.FA2_OK:
+        raise SystemExit("device status error during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        with torch.cuda.stream(stream):
+            t_begin.record(stream)
+            for i in range(args.steps):
+                if flush is not None:
+                    flush.zero_()
+                starts[i].record(stream)
+                step(stream)
+                ends[i].record(stream)
+            t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    if fa2.fa2_device_status(None, reset=True) != fa2.FA2_OK:
+        raise SystemExit("device status error in the timed region")
+    launch_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    timed_ms = sum(launch_ms) if flush is not None else t_begin.elapsed_time(t_end)
+    job_ms = job_time_ms(timed_ms, dist, dev)
+    flops = 2.5 * w.flops
+
+    # end to end through the public calls: pinned inputs in, gradients out, every step
+    pins = [t.pin_memory() for t in (Qh, Kh, Vh, Gh)]
+    Oh, Lh = O.cpu().pin_memory(), L.cpu().pin_memory()
+    outs = [torch.empty(t.shape, dtype=torch.float32).pin_memory() for t in (dQ, dK, dV)]
+
+    def e2e_step():
+        for dst, src in zip((Q, K, V, G, O, L), pins + [Oh, Lh]):
+            dst.copy_(src, non_blocking=True)
+        step(stream)
+        for dst, src in zip(outs, (dQ, dK, dV)):
+            dst.copy_(src, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = job_time_ms(e0.elapsed_time(e1), dist, dev)
+    h2d = sum(t.numel() * t.element_size() for t in pins + [Oh, Lh])
+    d2h = sum(t.numel() * 4 for t in outs)
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    mean_launch_ms = statistics.mean(launch_ms)
+    achieved = flops / (mean_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    algo = algorithmic_bytes_backward(w)
+    hbm_bound = flops / algo < peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    cpu = None
+    if args.cpu_baseline_s > 0:
+        tf, cores, n, el = oracle_backward_rate(w, Qh, Kh, Vh, Gh, args.cpu_baseline_s)
+        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"head 0 of {w.name} truncated to its leading {n} queries and keys in "
+                         f"{el:.1f} s (fp64 oracle backward, FLOPs = 2.5 x the forward's)"}
+    value = job_tflops(flops, args.steps, world, job_ms)
+    line = {
+        "metric": METRIC_BWD,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(job_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(workload_config(w, l2_note), **{
+            "pass": "backward", "inputs": "bf16 Q, K, V, dO; fp32 O, LSE",
+            "outputs": "fp32 dQ, dK, dV"}),
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "roofline": roofline_entry(hbm_bound, achieved, peak, peak_src, peaks,
+                                   recorded_traffic(w.name + ":backward", BWD_KERNEL_SOURCES),
+                                   flops, algo, mean_launch_ms, kernel="fa2dev::fa2_bwd_tc_kernel"),
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(job_tflops(flops, args.e2e_steps, world, e2e_ms), 2),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * 2,
+        "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
     if dist:

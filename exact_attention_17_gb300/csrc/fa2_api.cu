@@ -116,6 +116,21 @@ bool encode_map(CUtensorMap* map, const void* base, int d, int N, int BH, bool f
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over an fp32 [BH][N][d] array: box = 32 columns (128 B) x 128 rows x 1,
+// 128-byte swizzle; the backward pass adds its dQ partials through it.
+bool encode_map_f32(CUtensorMap* map, const void* base, int d, int N, int BH) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = driver().encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
+                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 struct Problem {
   int B, H, Nq, Nk, d;
   long long BH;
@@ -395,11 +410,12 @@ extern "C" int fa2_backward(const void* Q, const void* K, const void* V, const f
       !device_range_ok(workspace, need))
     return FA2_ERR_MEMORY;
 
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!encode_map(&mq, Q, d, Nq, static_cast<int>(BH), false) ||
       !encode_map(&mk, K, d, Nk, static_cast<int>(BH), false) ||
       !encode_map(&mv, V, d, Nk, static_cast<int>(BH), false) ||
-      !encode_map(&mdo, dO, d, Nq, static_cast<int>(BH), false))
+      !encode_map(&mdo, dO, d, Nq, static_cast<int>(BH), false) ||
+      !encode_map_f32(&mdq, dQ, d, Nq, static_cast<int>(BH)))
     return FA2_ERR_SHAPE;
 
   const int Nq_pad = (Nq + 127) / 128 * 128;
@@ -431,7 +447,7 @@ extern "C" int fa2_backward(const void* Q, const void* K, const void* V, const f
     return FA2_ERR_LAUNCH;
   const long long grid = BH * p.key_blocks;
   if (grid > 0x7fffffffLL) return FA2_ERR_SHAPE;
-  return fa2host::launch_bwd(d, causal != 0, mq, mk, mv, mdo, p, static_cast<unsigned>(grid), s) ==
+  return fa2host::launch_bwd(d, causal != 0, mq, mk, mv, mdo, mdq, p, static_cast<unsigned>(grid), s) ==
                  cudaSuccess
              ? FA2_OK
              : FA2_ERR_LAUNCH;

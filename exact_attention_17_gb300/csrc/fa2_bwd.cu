@@ -28,12 +28,13 @@ cudaError_t set_limits_bwd() {
 
 template <int D>
 void run_bwd(bool causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-             const CUtensorMap& mdo, const fa2dev::BwdParams& p, unsigned grid, cudaStream_t s) {
+             const CUtensorMap& mdo, const CUtensorMap& mdq, const fa2dev::BwdParams& p, unsigned grid,
+             cudaStream_t s) {
   constexpr uint32_t smem = fa2dev::BwdConfig<D>::kSmemBytes;
   if (causal)
-    fa2dev::fa2_bwd_tc_kernel<D, true, false><<<grid, fa2dev::kBwdThreads, smem, s>>>(mq, mk, mv, mdo, p);
+    fa2dev::fa2_bwd_tc_kernel<D, true, false><<<grid, fa2dev::kBwdThreads, smem, s>>>(mq, mk, mv, mdo, mdq, p);
   else
-    fa2dev::fa2_bwd_tc_kernel<D, false, false><<<grid, fa2dev::kBwdThreads, smem, s>>>(mq, mk, mv, mdo, p);
+    fa2dev::fa2_bwd_tc_kernel<D, false, false><<<grid, fa2dev::kBwdThreads, smem, s>>>(mq, mk, mv, mdo, mdq, p);
 }
 }  // namespace
 
@@ -43,12 +44,12 @@ cudaError_t prepare_bwd() {
 }
 
 cudaError_t launch_bwd(int d, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const CUtensorMap& mdo, const fa2dev::BwdParams& p,
-                       unsigned grid, cudaStream_t s) {
+                       const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
+                       const fa2dev::BwdParams& p, unsigned grid, cudaStream_t s) {
   if (d == 64)
-    run_bwd<64>(causal, mq, mk, mv, mdo, p, grid, s);
+    run_bwd<64>(causal, mq, mk, mv, mdo, mdq, p, grid, s);
   else
-    run_bwd<128>(causal, mq, mk, mv, mdo, p, grid, s);
+    run_bwd<128>(causal, mq, mk, mv, mdo, mdq, p, grid, s);
   return cudaGetLastError();
 }
 

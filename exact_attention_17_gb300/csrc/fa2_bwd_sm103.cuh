@@ -23,8 +23,8 @@
 //      dQ_i = dS K_j      (dS from shared memory, MN-major; TMEM over S^T)
 //    and eight warps (two warpgroups, each owning half of a key row's query
 //    columns -- the backward needs no row reductions) turn S^T into P^T and
-//    dP^T into dS^T, then add the dQ_i partial into global memory with
-//    vector float reductions;
+//    dP^T into dS^T, then stage the dQ_i partial in shared memory and add it
+//    into global memory with TMA bulk reductions;
 //  * dK and dV stay in TMEM for the whole CTA and are stored once;
 //  * every mbarrier wait is bounded as in the forward kernel.
 #pragma once
@@ -81,7 +81,8 @@ template <int STAGES>
 struct alignas(8) BwdBarriers {
   uint64_t kv_full;
   uint64_t q_full[STAGES];
-  uint64_t q_empty[STAGES];
+  uint64_t q_empty[STAGES];   // one arrival per warpgroup once its dQ staging was read
+  uint64_t dq_staged[2];      // per warpgroup: its 128 threads wrote their dQ rows
   uint64_t s_full;
   uint64_t p_ready;
   uint64_t ds_ready;
@@ -137,12 +138,6 @@ __global__ void __launch_bounds__(256) fa2_bwd_pre_kernel(const float* __restric
   }
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -154,12 +149,26 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// TMA element-wise add of a shared-memory box into global memory (fp32).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                                  int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa2_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                      const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using Cfg = BwdConfig<D>;
   constexpr int STAGES = Cfg::kStages;
   constexpr uint32_t TILE = Cfg::kTileBytes;
@@ -202,8 +211,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bar_init(&bars->kv_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       bar_init(&bars->q_full[s], 1);
-      bar_init(&bars->q_empty[s], 1);
+      bar_init(&bars->q_empty[s], 2);
     }
+    bar_init(&bars->dq_staged[0], 128);
+    bar_init(&bars->dq_staged[1], 128);
     bar_init(&bars->s_full, 1);
     bar_init(&bars->p_ready, 256);
     bar_init(&bars->ds_ready, 256);
@@ -307,7 +318,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_ss(tmem + Cfg::kColS, sdesc_sw128(adS + kk * 2048, kChunkBytes, 1024),
                    sdesc_sw128(aK + kk * 2048, kChunkBytes, 1024), kIdDq, kk > 0 ? 1u : 0u);
           mma_commit(&bars->dq_full);
-          mma_commit(&bars->q_empty[slot]);
         }
         if (!ok) raise_abort(abort, p.status);
         mma_commit(&bars->mma_drain);
@@ -328,9 +338,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float* Drh = p.Dr + static_cast<size_t>(bh) * p.Nq_pad;
     const uint32_t ds_base = smem_addr(sdS) + wg * kChunkBytes + row * 128;
     bool ok = true;
+    const bool leader = (threadIdx.x & 127) == 0;
     for (int t = 0; t < n_tiles; ++t) {
+      const int slot = t % STAGES;
       const int qbase = (i0 + t) * 128;
       const int qcol0 = qbase + 64 * wg;      // first query of this warpgroup's columns
+      // this tile's LSE log2(e) for the warpgroup's columns, fetched while S^T is computed
+      float4 l4v[16];
+#pragma unroll
+      for (int e4 = 0; e4 < 16; ++e4) l4v[e4] = __ldg(reinterpret_cast<const float4*>(L2h + qcol0) + e4);
       if (!__all_sync(0xffffffffu, wait_bar(&bars->s_full, t & 1, abort, p.timeout_ns))) {
         ok = false;
         break;
@@ -344,10 +360,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t s[32];
         tmem_ld32(tmem + lane_bits + Cfg::kColS + 64 * wg + 32 * h, s);
         tmem_ld_wait(s);
-        const float4* l4 = reinterpret_cast<const float4*>(L2h + qcol0 + 32 * h);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l = __ldg(l4 + e4);
+          const float4 l = l4v[8 * h + e4];
           const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -361,6 +376,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int e = 0; e < 32; ++e) pk[e] = pack_x2<F16>(P[2 * e], P[2 * e + 1]);
       tmem_st32(tmem + lane_bits + Cfg::kColS + 64 * wg, pk);
+      // D for the same columns, fetched while the P^T store completes
+      float4 d4v[16];
+#pragma unroll
+      for (int e4 = 0; e4 < 16; ++e4) d4v[e4] = __ldg(reinterpret_cast<const float4*>(Drh + qcol0) + e4);
       tmem_st_wait();
       tc_fence_before_sync();
       bar_arrive(&bars->p_ready);
@@ -371,10 +390,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t g[32];
         tmem_ld32(tmem + lane_bits + Cfg::kColDP + 64 * wg + 32 * h, g);
         tmem_ld_wait(g);
-        const float4* d4 = reinterpret_cast<const float4*>(Drh + qcol0 + 32 * h);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 dv = __ldg(d4 + e4);
+          const float4 dv = d4v[8 * h + e4];
           const float dd[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
           for (int u = 0; u < 4; u += 2) {
@@ -398,30 +416,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before_sync();
       bar_arrive(&bars->ds_ready);
 
-      // dQ_i partial (TMEM lanes are query rows now): scale it and add it in
+      // dQ_i partial (TMEM lanes are query rows now).  Its columns go back to
+      // the issuer as soon as they are in registers; the scaled rows are then
+      // staged in this tile's Q/dO ring slot (no MMA reads it any more) as
+      // 128-byte-swizzled boxes of 32 columns, and one thread per warpgroup
+      // adds them into dQ with TMA reductions before releasing the slot.
       if (!__all_sync(0xffffffffu, wait_bar(&bars->dq_full, t & 1, abort, p.timeout_ns))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const int q = qbase + row;
+      uint32_t v[D / 64][32];
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = (D / 2) * wg + 32 * c;
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_bits + Cfg::kColS + col, v);
-        tmem_ld_wait(v);
-        if (q < p.Nq) {
-          float* dst = p.dQ + (static_cast<size_t>(bh) * p.Nq + q) * D + col;
+      for (int c = 0; c < D / 64; ++c) tmem_ld32(tmem + lane_bits + Cfg::kColS + (D / 2) * wg + 32 * c, v[c]);
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            red_add_v4(dst + e, __uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
-                       __uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale);
-        }
-      }
+      for (int c = 0; c < D / 64; ++c) tmem_ld_wait(v[c]);
       tc_fence_before_sync();
       bar_arrive(&bars->dq_free);
+      uint8_t* stage = wg == 0 ? sQ + slot * TILE : sdO + slot * TILE;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const uint32_t box = smem_addr(stage) + c * 16384 + row * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(box + ((u ^ (row & 7)) << 4), __float_as_uint(__uint_as_float(v[c][4 * u]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[c][4 * u + 1]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[c][4 * u + 2]) * p.scale),
+                       __float_as_uint(__uint_as_float(v[c][4 * u + 3]) * p.scale));
+      }
+      fence_proxy_async_shared();
+      bar_arrive(&bars->dq_staged[wg]);
+      if (leader) {
+        if (!wait_bar(&bars->dq_staged[wg], t & 1, abort, p.timeout_ns)) {
+          ok = false;
+        } else {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_reduce_add_3d(&tm_dq, stage + c * 16384, (D / 2) * wg + 32 * c, qbase, bh);
+          bulk_commit();
+          bulk_wait_read();
+          bar_arrive(&bars->q_empty[slot]);
+        }
+      }
+      // keep `ok` uniform across the warp: the TMEM accesses after the loop are warp-collective
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
     }
+    if (leader) bulk_wait_all();
 
     // dK = scale dS^T Q and dV = P^T dO for this CTA's keys (zero when no query
     // sees them).  `ok` and n_tiles are uniform across a warp; the TMEM loads
