@@ -383,6 +383,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       tc_fence_before_sync();
       bar_arrive(&bars->p_ready);
+      // the previous tile's dQ reductions have had a whole P phase to read
+      // their staging: release that ring slot to the producer now
+      if (leader && t > 0) {
+        bulk_wait_read();
+        bar_arrive(&bars->q_empty[(t - 1) % STAGES]);
+      }
 
       // dS^T = P^T (dP^T - D): to TMEM (A of dK) and to shared memory (A of dQ)
 #pragma unroll
@@ -454,14 +460,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int c = 0; c < D / 64; ++c)
             tma_reduce_add_3d(&tm_dq, stage + c * 16384, (D / 2) * wg + 32 * c, qbase, bh);
           bulk_commit();
-          bulk_wait_read();
-          bar_arrive(&bars->q_empty[slot]);
         }
       }
       // keep `ok` uniform across the warp: the TMEM accesses after the loop are warp-collective
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
     }
+    // the last tile's reductions must complete before the CTA exits
     if (leader) bulk_wait_all();
 
     // dK = scale dS^T Q and dV = P^T dO for this CTA's keys (zero when no query
