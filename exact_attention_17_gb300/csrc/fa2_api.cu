@@ -131,6 +131,28 @@ bool encode_map_f32(CUtensorMap* map, const void* base, int d, int N, int BH) {
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over the forward's output [Z][Nq][d] (Z = B*H, or splits * B*H for
+// the split-KV partials): fp32 with 32-column boxes, or 16-bit (bf16/fp16)
+// with 64-column boxes; 128 rows, 128-byte swizzle.  The epilogue stores O
+// through it; rows past Nq fall outside the map.
+bool encode_map_out(CUtensorMap* map, const void* base, int d, int Nq, long long Z, int elem_bytes,
+                    bool f16) {
+  if (Z > 0x7fffffffLL) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Nq),
+                        static_cast<cuuint64_t>(Z)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
+                           static_cast<cuuint64_t>(Nq) * d * elem_bytes};
+  cuuint32_t box[3] = {elem_bytes == 4 ? 32u : 64u, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType type = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : f16           ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = driver().encode(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 struct Problem {
   int B, H, Nq, Nk, d;
   long long BH;
@@ -199,10 +221,13 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   const long long blocks = (static_cast<long long>(Nq) + 128 * subs - 1) / (128 * subs);
   if (blocks * pr.BH * splits > 0x7fffffffLL) return FA2_ERR_SHAPE;
 
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
+  const bool split_out = splits > 1;
   if (!encode_map(&mq, Q, d, Nq, static_cast<int>(pr.BH), f16) ||
       !encode_map(&mk, K, d, Nk, static_cast<int>(pr.BH), f16) ||
-      !encode_map(&mv, V, d, Nk, static_cast<int>(pr.BH), f16))
+      !encode_map(&mv, V, d, Nk, static_cast<int>(pr.BH), f16) ||
+      !encode_map_out(&mo, split_out ? static_cast<const void*>(O_part) : static_cast<const void*>(O), d, Nq,
+                      split_out ? pr.BH * splits : pr.BH, (o_half && !split_out) ? 2 : 4, f16))
     return FA2_ERR_SHAPE;
 
   fa2dev::FwdParams p;
@@ -227,11 +252,11 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   const bool c = causal != 0;
   cudaError_t e;
   if (d == 64)
-    e = f16 ? fa2host::launch_tc_d64_f16(subs, c, mq, mk, mv, p, grid, s)
-            : fa2host::launch_tc_d64_bf16(subs, c, mq, mk, mv, p, grid, s);
+    e = f16 ? fa2host::launch_tc_d64_f16(subs, c, mq, mk, mv, mo, p, grid, s)
+            : fa2host::launch_tc_d64_bf16(subs, c, mq, mk, mv, mo, p, grid, s);
   else
-    e = f16 ? fa2host::launch_tc_d128_f16(subs, c, mq, mk, mv, p, grid, s)
-            : fa2host::launch_tc_d128_bf16(subs, c, mq, mk, mv, p, grid, s);
+    e = f16 ? fa2host::launch_tc_d128_f16(subs, c, mq, mk, mv, mo, p, grid, s)
+            : fa2host::launch_tc_d128_bf16(subs, c, mq, mk, mv, mo, p, grid, s);
   return e == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
 }
 

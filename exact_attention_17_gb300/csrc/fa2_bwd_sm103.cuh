@@ -138,30 +138,6 @@ __global__ void __launch_bounds__(256) fa2_bwd_pre_kernel(const float* __restric
   }
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// TMA element-wise add of a shared-memory box into global memory (fp32).
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x, int y,
-                                                  int z) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa2_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,

@@ -128,6 +128,8 @@ struct alignas(8) FwdBarriers {
   uint64_t s_full[2];
   uint64_t p_ready[2];
   uint64_t o_done[2];
+  uint64_t staged[2];      // epilogue: a sub-tile's 128 threads wrote O into its Q buffer
+  uint64_t stage_free[2];  // epilogue: the TMA stores have read that buffer
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort;
@@ -157,7 +159,8 @@ template <int D, bool CAUSAL, bool F16, int SUBS>
 __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCtasPerSm)
     fa2_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using Cfg = FwdConfig<D, SUBS>;
   using Shape = FwdShape<SUBS>;
   constexpr int kWarpProducer = 4 * SUBS;      // TMA warp
@@ -215,6 +218,8 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
       bar_init(&bars->s_full[i], 1);
       bar_init(&bars->p_ready[i], kRowsPerSub);
       bar_init(&bars->o_done[i], 1);
+      bar_init(&bars->staged[i], kRowsPerSub);
+      bar_init(&bars->stage_free[i], 1);
     }
     bar_init(&bars->mma_drain, 1);
     bars->abort = 0;
@@ -489,32 +494,73 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         ok = false;
       } else {
         tc_fence_after_sync();
+        // O / l is written into this sub-tile's Q buffer (every S MMA that
+        // read it has completed) as 128-byte-swizzled boxes, which one thread
+        // stores with TMA; rows past Nq fall outside the map and are dropped.
+        // fp32 O takes two rounds of D/2 columns (boxes of 32 columns), O in
+        // the input type one round (boxes of 64 columns).
         // l == 0 only for a row whose every key in this range is masked
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait(o);
-          if (store && !half_out) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              float4 v = make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
-                                     __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
-              *reinterpret_cast<float4*>(orow + c * 32 + e) = v;
-            }
-          } else if (store) {
-            // O in the input element type: 32 values -> 64 bytes
-            uint32_t h[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              h[e >> 1] = pack_x2<F16>(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.O) + row_id * D + c * 32);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
+        uint8_t* stage = sQ + sub * TILE;
+        const uint32_t stage_row = smem_addr(stage) + row * 128;
+        const int zrow = (p.num_splits > 1 ? split * p.BH : 0) + bh;
+        const bool leader = (threadIdx.x & (kRowsPerSub - 1)) == 0;
+        const int rounds = half_out ? 1 : 2;
+        for (int r = 0; r < rounds && ok; ++r) {
+          if (r > 0 && !__all_sync(0xffffffffu, wait_bar(&bars->stage_free[sub], 0, abort, p.timeout_ns))) {
+            ok = false;
+            break;
           }
+#pragma unroll
+          for (int b = 0; b < D / 64; ++b) {
+            const uint32_t box = stage_row + b * 16384;
+            if (!half_out) {
+              uint32_t o[32];
+              tmem_ld32(tO + r * (D / 2) + 32 * b, o);
+              tmem_ld_wait(o);
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                st_shared_v4(box + ((u ^ (row & 7)) << 4), __float_as_uint(__uint_as_float(o[4 * u]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[4 * u + 1]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[4 * u + 2]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[4 * u + 3]) * inv_l));
+            } else {
+              uint32_t o[2][32];
+              tmem_ld32(tO + 64 * b, o[0]);
+              tmem_ld32(tO + 64 * b + 32, o[1]);
+              tmem_ld_wait(o[0]);
+              tmem_ld_wait(o[1]);
+              uint32_t h[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                h[e] = pack_x2<F16>(__uint_as_float(o[e >> 4][(2 * e) & 31]) * inv_l,
+                                    __uint_as_float(o[e >> 4][(2 * e + 1) & 31]) * inv_l);
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                st_shared_v4(box + ((u ^ (row & 7)) << 4), h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
+            }
+          }
+          fence_proxy_async_shared();
+          bar_arrive(&bars->staged[sub]);
+          if (leader) {
+            if (!wait_bar(&bars->staged[sub], r & 1, abort, p.timeout_ns)) {
+              ok = false;
+            } else {
+#pragma unroll
+              for (int b = 0; b < D / 64; ++b)
+                tma_store_3d(&tm_o, stage + b * 16384, half_out ? 64 * b : r * (D / 2) + 32 * b, sub_row0, zrow);
+              bulk_commit();
+              if (r + 1 < rounds) {
+                bulk_wait_read();
+                bar_arrive(&bars->stage_free[sub]);
+              }
+            }
+          }
+          ok = __all_sync(0xffffffffu, ok);
         }
         if (store) *lse_out = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        // the stores must be complete before the CTA exits
+        if (leader) bulk_wait_all();
       }
     }
     if (!ok) raise_abort(abort, p.status);

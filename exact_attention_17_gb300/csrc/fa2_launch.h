@@ -18,11 +18,12 @@ cudaError_t prepare_tc_d64_f16();
 cudaError_t prepare_tc_d128_f16();
 cudaError_t prepare_simt();
 
-// subs: query sub-tiles of 128 rows per CTA (1 or 2).
+// subs: query sub-tiles of 128 rows per CTA (1 or 2).  mo: the map the epilogue stores O (or
+// the split-KV partial O) through.
 #define FA2_DECLARE_TC_LAUNCH(name)                                                          \
   cudaError_t name(int subs, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,      \
-                   const CUtensorMap& mv, const fa2dev::FwdParams& p, unsigned grid,         \
-                   cudaStream_t s);
+                   const CUtensorMap& mv, const CUtensorMap& mo, const fa2dev::FwdParams& p, \
+                   unsigned grid, cudaStream_t s);
 FA2_DECLARE_TC_LAUNCH(launch_tc_d64_bf16)
 FA2_DECLARE_TC_LAUNCH(launch_tc_d128_bf16)
 FA2_DECLARE_TC_LAUNCH(launch_tc_d64_f16)

@@ -17,13 +17,13 @@ cudaError_t set_limits() {
 
 template <int SUBS>
 cudaError_t run(bool causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                const fa2dev::FwdParams& p, unsigned grid, cudaStream_t s) {
+                const CUtensorMap& mo, const fa2dev::FwdParams& p, unsigned grid, cudaStream_t s) {
   constexpr uint32_t smem = fa2dev::FwdConfig<128, SUBS>::kSmemBytes;
   constexpr int threads = fa2dev::FwdShape<SUBS>::kThreads;
   if (causal)
-    fa2dev::fa2_fwd_tc_kernel<128, true, true, SUBS><<<grid, threads, smem, s>>>(mq, mk, mv, p);
+    fa2dev::fa2_fwd_tc_kernel<128, true, true, SUBS><<<grid, threads, smem, s>>>(mq, mk, mv, mo, p);
   else
-    fa2dev::fa2_fwd_tc_kernel<128, false, true, SUBS><<<grid, threads, smem, s>>>(mq, mk, mv, p);
+    fa2dev::fa2_fwd_tc_kernel<128, false, true, SUBS><<<grid, threads, smem, s>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 }  // namespace
@@ -34,9 +34,9 @@ cudaError_t prepare_tc_d128_f16() {
 }
 
 cudaError_t launch_tc_d128_f16(int subs, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
-                              const CUtensorMap& mv, const fa2dev::FwdParams& p, unsigned grid,
+                              const CUtensorMap& mv, const CUtensorMap& mo, const fa2dev::FwdParams& p, unsigned grid,
                               cudaStream_t s) {
-  return subs == 1 ? run<1>(causal, mq, mk, mv, p, grid, s) : run<2>(causal, mq, mk, mv, p, grid, s);
+  return subs == 1 ? run<1>(causal, mq, mk, mv, mo, p, grid, s) : run<2>(causal, mq, mk, mv, mo, p, grid, s);
 }
 
 }  // namespace fa2host
