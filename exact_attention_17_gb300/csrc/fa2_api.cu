@@ -245,6 +245,7 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   p.LSE_part = LSE_part;
   p.o_half = o_half ? 1 : 0;
   p.item_group = item_group(pr, splits);
+  p.wave = sm_count() * (subs == 2 ? 1 : 2);
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
     return FA2_ERR_LAUNCH;
 

@@ -63,6 +63,7 @@ struct FwdParams {
   int q_blocks;    // ceil(Nq / rows per CTA)
   float scale_log2;  // scale * log2(e)
   int* status;     // device status word
+  int wave;        // CTAs that run at once (the L2 prefetch looks one wave ahead)
   unsigned long long timeout_ns;
   // Split of the keys into ranges processed by separate CTAs ("FlashDecoding",
   // "Flash Attention 全解析(上)" section 4): range s covers key tiles
@@ -208,7 +209,12 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
   const int nmax = max(n0, n1);
   const int q_row0 = u * SUBS * kRowsPerSub;
 
-  if (threadIdx.x == 0) {
+  // The producer thread sets up the barriers and starts the first loads (Q
+  // and the first ring slots) before the CTA-wide synchronisation, so that
+  // their latency overlaps the TMEM allocation and the synchronisation.
+  const uint32_t qbytes = (n0 > 0 ? TILE : 0u) + (n1 > 0 ? TILE : 0u);
+  const int primed = min(STAGES, 2 * nmax);   // K/V loads issued before the synchronisation
+  if (warp == kWarpProducer && lane == 0) {
     bar_init(&bars->q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       bar_init(&bars->kv_full[s], 1);
@@ -224,6 +230,42 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
     bar_init(&bars->mma_drain, 1);
     bars->abort = 0;
     fence_barrier_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    if (qbytes) {
+      bar_arrive_expect_tx(&bars->q_full, qbytes);
+      for (int s = 0; s < SUBS; ++s) {
+        if ((s == 0 ? n0 : n1) == 0) continue;
+        for (int c = 0; c < NCH; ++c)
+          tma_load_3d(sQ + s * TILE + c * kChunkBytes, &tm_q, &bars->q_full, c * 64,
+                      q_row0 + s * kRowsPerSub, bh);
+      }
+    }
+    for (int g = 0; g < primed; ++g) {
+      bar_arrive_expect_tx(&bars->kv_full[g], TILE);
+      const CUtensorMap* map = (g & 1) == 0 ? &tm_k : &tm_v;
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d(sKV + g * TILE + c * kChunkBytes, map, &bars->kv_full[g], c * 64,
+                    (t_begin + g / 2) * kKeysPerTile, bh);
+    }
+    // The CTA one wave later (probably the next to run on some SM) reads a Q
+    // block nobody has touched yet: start bringing it into L2 now.
+    const unsigned later = blockIdx.x + p.wave;
+    if (later < gridDim.x) {
+      const int item2 = static_cast<int>(later);
+      const int group2 = item2 / per_group;
+      const int in_group2 = item2 - group2 * per_group;
+      const int gi2 = min(p.item_group, items - group2 * p.item_group);
+      const int u_rank2 = in_group2 / gi2;
+      const int pair2 = group2 * p.item_group + (in_group2 - u_rank2 * gi2);
+      const int u2 = CAUSAL ? U - 1 - u_rank2 : u_rank2;
+      const int row2 = u2 * SUBS * kRowsPerSub;
+      for (int s = 0; s < SUBS; ++s)
+        if (row2 + s * kRowsPerSub < p.Nq)
+          for (int c = 0; c < NCH; ++c)
+            tma_prefetch_l2_3d(&tm_q, c * 64, row2 + s * kRowsPerSub, pair2 / p.num_splits);
+    }
   }
   if (warp == kWarpMma) {
     tmem_alloc(&bars->tmem_base, Cfg::kTmemCols);
@@ -241,21 +283,11 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
     if (warp == kWarpProducer) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
-        const uint32_t qbytes = (n0 > 0 ? TILE : 0u) + (n1 > 0 ? TILE : 0u);
-        bar_arrive_expect_tx(&bars->q_full, qbytes);
-        for (int s = 0; s < SUBS; ++s) {
-          if ((s == 0 ? n0 : n1) == 0) continue;
-          for (int c = 0; c < NCH; ++c)
-            tma_load_3d(sQ + s * TILE + c * kChunkBytes, &tm_q, &bars->q_full, c * 64,
-                        q_row0 + s * kRowsPerSub, bh);
-        }
-        int issued = 0;
+        // Q and the first `primed` K/V loads were issued before the synchronisation
+        int issued = primed;
         bool ok = true;
-        for (int j = 0; j < nmax && ok; ++j) {
-          for (int kind = 0; kind < 2; ++kind) {
+        for (int j = primed / 2; j < nmax && ok; ++j) {
+          for (int kind = (primed & 1) && j == primed / 2 ? 1 : 0; kind < 2; ++kind) {
             const int slot = issued % STAGES;
             const int round = issued / STAGES;
             if (round > 0 && !wait_bar(&bars->kv_empty[slot], (round - 1) & 1, abort, p.timeout_ns)) {
