@@ -318,25 +318,35 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         const uint32_t sQaddr = smem_addr(sQ);
         const uint32_t sKVaddr = smem_addr(sKV);
 
+        // Descriptors are formed once per operand tile and advanced by adding
+        // the K-step offset to the start-address field: shared addresses are
+        // below 256 KB and multiples of 16, so the 14-bit field cannot carry.
+        // Fewer instructions per MMA matter here: any pause of this thread
+        // idles the tensor pipe.
         // S_sub = Q_sub K^T : K-major A and B, K = D in steps of 16.
         auto issue_s = [&](int sub, int slot) {
-          const uint32_t a0 = sQaddr + sub * TILE;
-          const uint32_t b0 = sKVaddr + slot * TILE;
+          uint64_t da = sdesc_sw128(sQaddr + sub * TILE, 16, 1024);
+          uint64_t db = sdesc_sw128(sKVaddr + slot * TILE, 16, 1024);
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem + sub * 128, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
-                   kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + sub * 128, da, db, kIdescS, kk > 0 ? 1u : 0u);
+            // next K step: 32 bytes within a 128-byte swizzle atom, else the next 64-column chunk
+            const uint32_t step = ((kk & 3) == 3 ? kChunkBytes - 3 * 32 : 32) >> 4;
+            da += step;
+            db += step;
+            asm volatile("" : "+l"(da), "+l"(db));   // one step at a time: keeps two registers live
           }
         };
         // O_sub (+)= P_sub V : P from TMEM (bf16, 2 per column), V MN-major.
         auto issue_pv = [&](int sub, int slot, bool acc) {
-          const uint32_t b0 = sKVaddr + slot * TILE;
+          uint64_t dv = sdesc_sw128(sKVaddr + slot * TILE, kChunkBytes, 1024);
           const uint32_t o = tmem + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
+          const uint32_t a = tmem + sub * 128;
   #pragma unroll
           for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
-            mma_ts(o, tmem + sub * 128 + kk * 8, sdesc_sw128(b0 + kk * 16 * 128, kChunkBytes, 1024),
-                   kIdescO, (acc || kk > 0) ? 1u : 0u);
+            mma_ts(o, a + kk * 8, dv, kIdescO, (acc || kk > 0) ? 1u : 0u);
+            dv += (16 * 128) >> 4;   // next 16 keys of V
+            asm volatile("" : "+l"(dv));
           }
         };
 
