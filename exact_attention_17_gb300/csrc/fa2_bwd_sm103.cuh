@@ -253,23 +253,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         constexpr uint32_t kIdDq = idesc_f32acc(128, D, true, true, F16);       // dQ
         const uint32_t aK = smem_addr(sK), aV = smem_addr(sV);
         const uint32_t aQ = smem_addr(sQ), adO = smem_addr(sdO), adS = smem_addr(sdS);
+        // Descriptors are formed once per operand tile and stepped by the
+        // K-step offset (start-address field; shared addresses stay below
+        // 256 KB, so it cannot carry), one step at a time.
         // D[128 x 128] = A B^T with A, B K-major 128 x D tiles
         auto issue_kmajor = [&](uint32_t dcol, uint32_t a0, uint32_t b0) {
+          uint64_t da = sdesc_sw128(a0, 16, 1024), db = sdesc_sw128(b0, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem + dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
-                   kIdSq, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + dcol, da, db, kIdSq, kk > 0 ? 1u : 0u);
+            const uint32_t step = ((kk & 3) == 3 ? kChunkBytes - 3 * 32 : 32) >> 4;
+            da += step;
+            db += step;
+            asm volatile("" : "+l"(da), "+l"(db));
           }
         };
         // D[128 x D] (+)= A[tmem, 128 x 128] B, B an MN-major 128 x D tile; the
         // A columns of warpgroup w's queries start at acol + 64 w.
         auto issue_ts = [&](uint32_t dcol, uint32_t acol, uint32_t b0, bool acc) {
+          uint64_t dbv = sdesc_sw128(b0, kChunkBytes, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t a = tmem + acol + 64 * (kk >> 2) + 8 * (kk & 3);
-            mma_ts(tmem + dcol, a, sdesc_sw128(b0 + kk * 2048, kChunkBytes, 1024), kIdAcc,
-                   (acc || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + dcol, a, dbv, kIdAcc, (acc || kk > 0) ? 1u : 0u);
+            dbv += 2048 >> 4;
+            asm volatile("" : "+l"(dbv));
           }
         };
         bool ok = wait_bar(&bars->kv_full, 0, abort, p.timeout_ns);
@@ -289,10 +297,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!wait_bar(&bars->ds_ready, t & 1, abort, p.timeout_ns)) { ok = false; break; }
           tc_fence_after_sync();
           issue_ts(Cfg::kColDK, Cfg::kColDP, q0, t > 0);            // dK += dS^T Q
+          {                                                          // dQ_i = dS K
+            uint64_t dA = sdesc_sw128(adS, kChunkBytes, 1024), dB = sdesc_sw128(aK, kChunkBytes, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)                            // dQ_i = dS K
-            mma_ss(tmem + Cfg::kColS, sdesc_sw128(adS + kk * 2048, kChunkBytes, 1024),
-                   sdesc_sw128(aK + kk * 2048, kChunkBytes, 1024), kIdDq, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              mma_ss(tmem + Cfg::kColS, dA, dB, kIdDq, kk > 0 ? 1u : 0u);
+              dA += 2048 >> 4;
+              dB += 2048 >> 4;
+              asm volatile("" : "+l"(dA), "+l"(dB));
+            }
+          }
           mma_commit(&bars->dq_full);
         }
         if (!ok) raise_abort(abort, p.status);
