@@ -68,6 +68,7 @@ int device_ready() {
     if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return;
     if (fa2host::prepare_tc_d64_bf16() != cudaSuccess || fa2host::prepare_tc_d128_bf16() != cudaSuccess ||
         fa2host::prepare_tc_d64_f16() != cudaSuccess || fa2host::prepare_tc_d128_f16() != cudaSuccess ||
+        fa2host::prepare_tc_d256_bf16() != cudaSuccess || fa2host::prepare_tc_d256_f16() != cudaSuccess ||
         fa2host::prepare_simt() != cudaSuccess || fa2host::prepare_bwd() != cudaSuccess)
       return;
     st.usable = true;
@@ -153,6 +154,9 @@ bool encode_map_out(CUtensorMap* map, const void* base, int d, int Nq, long long
   return r == CUDA_SUCCESS;
 }
 
+// Head dimensions of the tensor-core forward kernels (and of the merge).
+bool forward_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+
 struct Problem {
   int B, H, Nq, Nk, d;
   long long BH;
@@ -168,7 +172,7 @@ int validate(const void* Q, const void* K, const void* V, const void* O, const f
   if (pr->empty) return FA2_OK;
   if (Nk < 1) return FA2_ERR_SHAPE;
   if (pr->BH > 0x7fffffffLL) return FA2_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA2_ERR_HEADDIM;
+  if (!forward_head_dim(d)) return FA2_ERR_HEADDIM;
   if (!(scale > 0.f) || !std::isfinite(scale)) return FA2_ERR_SCALE;
   if (!Q || !K || !V || !O || !LSE) return FA2_ERR_NULL;
   const uintptr_t a16 = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
@@ -192,7 +196,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // CTAs per SM) when a second sub-tile would have no rows (Nq <= 128) or when
 // two-sub-tile CTAs would not fill two waves of the GPU.
 int subtiles_per_cta(const Problem& pr, int splits) {
-  if (pr.Nq <= 128) return 1;
+  if (pr.Nq <= 128 || pr.d == 256) return 1;
   const long long ctas2 = (static_cast<long long>(pr.Nq) + 255) / 256 * pr.BH * splits;
   return ctas2 < 2LL * sm_count() ? 1 : 2;
 }
@@ -245,7 +249,7 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   p.LSE_part = LSE_part;
   p.o_half = o_half ? 1 : 0;
   p.item_group = item_group(pr, splits);
-  p.wave = sm_count() * (subs == 2 ? 1 : 2);
+  p.wave = sm_count() * (subs == 2 || d == 256 ? 1 : 2);
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
     return FA2_ERR_LAUNCH;
 
@@ -255,9 +259,12 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   if (d == 64)
     e = f16 ? fa2host::launch_tc_d64_f16(subs, c, mq, mk, mv, mo, p, grid, s)
             : fa2host::launch_tc_d64_bf16(subs, c, mq, mk, mv, mo, p, grid, s);
-  else
+  else if (d == 128)
     e = f16 ? fa2host::launch_tc_d128_f16(subs, c, mq, mk, mv, mo, p, grid, s)
             : fa2host::launch_tc_d128_bf16(subs, c, mq, mk, mv, mo, p, grid, s);
+  else
+    e = f16 ? fa2host::launch_tc_d256_f16(subs, c, mq, mk, mv, mo, p, grid, s)
+            : fa2host::launch_tc_d256_bf16(subs, c, mq, mk, mv, mo, p, grid, s);
   return e == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
 }
 
@@ -313,7 +320,7 @@ extern "C" int fa2_forward_typed(const void* Q, const void* K, const void* V, vo
 }
 
 extern "C" size_t fa2_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
-  if (B < 0 || H < 0 || Nq < 0 || num_splits < 1 || (d != 64 && d != 128)) return 0;
+  if (B < 0 || H < 0 || Nq < 0 || num_splits < 1 || !forward_head_dim(d)) return 0;
   return workspace_bytes(static_cast<long long>(B) * H, Nq, d, num_splits);
 }
 
@@ -351,7 +358,7 @@ extern "C" int fa2_merge(const float* O_parts, const float* LSE_parts, int num_p
   if (rows < 0 || num_parts < 0) return FA2_ERR_SHAPE;
   if (rows == 0) return FA2_OK;
   if (num_parts < 1 || num_parts > kMaxSplits) return FA2_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA2_ERR_HEADDIM;
+  if (!forward_head_dim(d)) return FA2_ERR_HEADDIM;
   if (!O_parts || !LSE_parts || !O || !LSE) return FA2_ERR_NULL;
   if (((reinterpret_cast<uintptr_t>(O_parts) | reinterpret_cast<uintptr_t>(O)) & 15u) != 0 ||
       ((reinterpret_cast<uintptr_t>(LSE_parts) | reinterpret_cast<uintptr_t>(LSE)) & 3u) != 0)
@@ -374,6 +381,7 @@ extern "C" int fa2_forward_simt(const void* Q, const void* K, const void* V, flo
   Problem pr;
   int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr);
   if (rc != FA2_OK || pr.empty) return rc;
+  if (d == 256) return FA2_ERR_HEADDIM;   // the SIMT kernels cover 64 and 128
   if (pr.BH > 65535) return FA2_ERR_SHAPE;
   fa2dev::SimtParams p;
   p.Q = static_cast<const __nv_bfloat16*>(Q);
@@ -485,7 +493,7 @@ extern "C" const char* fa2_status_string(int status) {
     case FA2_ERR_NULL: return "a required pointer is NULL";
     case FA2_ERR_ALIGN: return "Q/K/V/O must be 16-byte aligned and LSE 4-byte aligned";
     case FA2_ERR_SHAPE: return "invalid or unsupported sizes";
-    case FA2_ERR_HEADDIM: return "unsupported head dimension (64 or 128)";
+    case FA2_ERR_HEADDIM: return "unsupported head dimension (forward 64, 128 or 256; backward and SIMT 64 or 128)";
     case FA2_ERR_LAUNCH: return "CUDA launch or call failed";
     case FA2_ERR_TIMEOUT: return "a kernel gave up waiting on an internal barrier";
     case FA2_ERR_SCALE: return "scale must be finite and > 0";

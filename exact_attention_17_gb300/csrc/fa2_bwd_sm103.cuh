@@ -456,8 +456,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
     }
-    // the last tile's reductions must complete before the CTA exits
-    if (leader) bulk_wait_all();
+    // The last tile's reductions must have read their staged dQ before the
+    // CTA exits; their global updates complete with the grid.
+    if (leader) bulk_wait_read();
 
     // dK = scale dS^T Q and dV = P^T dO for this CTA's keys (zero when no query
     // sees them).  `ok` and n_tiles are uniform across a warp; the TMEM loads

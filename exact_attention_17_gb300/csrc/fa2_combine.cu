@@ -44,10 +44,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
       if (ls == -INFINITY) continue;
       const float w = expf(ls - mx) * inv;
       const float* src = O_part + (s * R + r) * D + lane * V;
-      if constexpr (V == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] = fmaf(w, x.x, acc[0]); acc[1] = fmaf(w, x.y, acc[1]);
-        acc[2] = fmaf(w, x.z, acc[2]); acc[3] = fmaf(w, x.w, acc[3]);
+      if constexpr (V % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < V; q += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src + q);
+          acc[q] = fmaf(w, x.x, acc[q]); acc[q + 1] = fmaf(w, x.y, acc[q + 1]);
+          acc[q + 2] = fmaf(w, x.z, acc[q + 2]); acc[q + 3] = fmaf(w, x.w, acc[q + 3]);
+        }
       } else {
         const float2 x = *reinterpret_cast<const float2*>(src);
         acc[0] = fmaf(w, x.x, acc[0]); acc[1] = fmaf(w, x.y, acc[1]);
@@ -55,9 +58,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     }
   }
   float* dst = O + r * D + lane * V;
-  if constexpr (V == 4)
-    *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  else
+  if constexpr (V % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < V; q += 4)
+      *reinterpret_cast<float4*>(dst + q) = make_float4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
+  } else
     *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
   if (lane == 0) LSE[r] = sum > 0.f ? mx + logf(sum) : -INFINITY;
 }
@@ -74,8 +79,10 @@ cudaError_t launch_combine(int d, const float* O_part, const float* LSE_part, in
   const dim3 grid(static_cast<unsigned>(blocks));
   if (d == 64)
     fa2dev::fa2_combine_kernel<64><<<grid, fa2dev::kCombineWarps * 32, 0, s>>>(O_part, LSE_part, S, R, O, LSE);
-  else
+  else if (d == 128)
     fa2dev::fa2_combine_kernel<128><<<grid, fa2dev::kCombineWarps * 32, 0, s>>>(O_part, LSE_part, S, R, O, LSE);
+  else
+    fa2dev::fa2_combine_kernel<256><<<grid, fa2dev::kCombineWarps * 32, 0, s>>>(O_part, LSE_part, S, R, O, LSE);
   return cudaGetLastError();
 }
 

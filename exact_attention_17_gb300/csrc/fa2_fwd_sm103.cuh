@@ -108,17 +108,28 @@ constexpr float kRescaleLog2 = 8.0f;
 
 template <int D, int SUBS>
 struct FwdConfig {
+  static_assert(D == 64 || D == 128 || D == 256, "head dimension");
+  // D = 256: a Q sub-tile or a K/V tile is 64 KB, so one sub-tile per CTA,
+  // one CTA per SM and a two-slot ring (192 KB of shared memory).
+  static_assert(D < 256 || SUBS == 1, "head dimension 256 takes one sub-tile per CTA");
   static constexpr int kChunks = D / 64;                    // 128-byte swizzle atoms per row
   static constexpr uint32_t kTileBytes = kKeysPerTile * D * 2;  // one K or V tile, one Q sub-tile
   // K/V ring slots (K and V alternate); with two CTAs per SM each gets half
   // of the shared memory.
-  static constexpr int kStages = SUBS == 2 ? (D == 128 ? 4 : 8) : (D == 128 ? 2 : 5);
-  // TMEM columns: S of each sub-tile (128 fp32 columns), then O of each (D).
-  static constexpr uint32_t kColsO0 = SUBS * 128;
-  static constexpr uint32_t kColsO1 = SUBS * 128 + D;
-  static constexpr uint32_t kTmemCols = SUBS == 2 ? 512 : 256;
+  static constexpr int kStages = D == 256 ? 2 : SUBS == 2 ? (D == 128 ? 4 : 8) : (D == 128 ? 2 : 5);
+  // S buffers in TMEM.  With one CTA per SM (D = 256) the 512 columns hold
+  // two S buffers and O: S for the next key tile is computed into the other
+  // buffer while the softmax of the current one runs.  Otherwise one per
+  // sub-tile, and S of the next tile overwrites P once P V is issued.
+  static constexpr bool kDoubleS = D == 256;
+  // TMEM columns: S buffers (128 fp32 columns each), then O of each sub-tile (D).
+  static constexpr uint32_t kColsO0 = (kDoubleS ? 2 : SUBS) * 128;
+  static constexpr uint32_t kColsO1 = kColsO0 + D;
+  static constexpr uint32_t kTmemCols = (SUBS == 2 || D == 256) ? 512 : 256;
+  static_assert(kColsO0 + SUBS * D <= kTmemCols, "TMEM columns");
   static constexpr uint32_t kSmemData = (SUBS + kStages) * kTileBytes;
   static constexpr uint32_t kSmemBytes = kSmemData + 1024 /*align*/ + 1024 /*barriers*/;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 template <int STAGES>
@@ -323,13 +334,14 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         // below 256 KB and multiples of 16, so the 14-bit field cannot carry.
         // Fewer instructions per MMA matter here: any pause of this thread
         // idles the tensor pipe.
-        // S_sub = Q_sub K^T : K-major A and B, K = D in steps of 16.
-        auto issue_s = [&](int sub, int slot) {
+        // S_sub = Q_sub K^T into S buffer `buf` (by default the sub-tile's
+        // own): K-major A and B, K = D in steps of 16.
+        auto issue_s = [&](int sub, int slot, int buf) {
           uint64_t da = sdesc_sw128(sQaddr + sub * TILE, 16, 1024);
           uint64_t db = sdesc_sw128(sKVaddr + slot * TILE, 16, 1024);
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            mma_ss(tmem + sub * 128, da, db, kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + buf * 128, da, db, kIdescS, kk > 0 ? 1u : 0u);
             // next K step: 32 bytes within a 128-byte swizzle atom, else the next 64-column chunk
             const uint32_t step = ((kk & 3) == 3 ? kChunkBytes - 3 * 32 : 32) >> 4;
             da += step;
@@ -337,11 +349,11 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
             asm volatile("" : "+l"(da), "+l"(db));   // one step at a time: keeps two registers live
           }
         };
-        // O_sub (+)= P_sub V : P from TMEM (bf16, 2 per column), V MN-major.
-        auto issue_pv = [&](int sub, int slot, bool acc) {
+        // O_sub (+)= P_sub V : P from TMEM S buffer `buf` (bf16, 2 per column), V MN-major.
+        auto issue_pv = [&](int sub, int slot, bool acc, int buf) {
           uint64_t dv = sdesc_sw128(sKVaddr + slot * TILE, kChunkBytes, 1024);
           const uint32_t o = tmem + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
-          const uint32_t a = tmem + sub * 128;
+          const uint32_t a = tmem + buf * 128;
   #pragma unroll
           for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
             mma_ts(o, a + kk * 8, dv, kIdescO, (acc || kk > 0) ? 1u : 0u);
@@ -355,11 +367,41 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         if (ok) ok = wait_bar(&bars->kv_full[0], 0, abort, p.timeout_ns);
         if (ok) {
           tc_fence_after_sync();
-          if (n0 > 0) { issue_s(0, 0); mma_commit(&bars->s_full[0]); }
-          if (n1 > 0) { issue_s(1, 0); mma_commit(&bars->s_full[1]); }
+          if (n0 > 0) { issue_s(0, 0, 0); mma_commit(&bars->s_full[0]); }
+          if (n1 > 0) { issue_s(1, 0, 1); mma_commit(&bars->s_full[1]); }
           mma_commit(&bars->kv_empty[0]);
         }
-        for (int j = 0; j < nmax && ok; ++j) {
+        if constexpr (Cfg::kDoubleS) {
+          // One sub-tile, S double-buffered: S(j+1) goes to the tensor pipe as
+          // soon as K(j+1) has landed, ahead of P(j) V, so that the softmax of
+          // tile j overlaps it.  S(j+2) overwrites P(j) only after P(j) V,
+          // which was issued before it.
+          for (int j = 0; j < n0 && ok; ++j) {
+            const int iv = 2 * j + 1, ik = 2 * j + 2;
+            const int slot_v = iv % STAGES, slot_k = ik % STAGES;
+            if (j + 1 < n0) {
+              if (!wait_bar(&bars->kv_full[slot_k], (ik / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
+              tc_fence_after_sync();
+              issue_s(0, slot_k, (j + 1) & 1);
+              mma_commit(&bars->s_full[(j + 1) & 1]);
+              mma_commit(&bars->kv_empty[slot_k]);
+            }
+            uint64_t* bv = &bars->kv_full[slot_v];
+            const uint32_t pv = (iv / STAGES) & 1;
+            // P(j) is announced on p_ready[j % 2]: a softmax that has already
+            // finished tile j + 1 cannot complete a second phase of the
+            // barrier waited on here.
+            if (!wait_bar3(bv, pv, &bars->p_ready[j & 1], (j >> 1) & 1, bv, pv, abort, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_pv(0, slot_v, j > 0, j & 1);
+            mma_commit(&bars->o_done[0]);
+            mma_commit(&bars->kv_empty[slot_v]);
+          }
+        }
+        for (int j = 0; j < nmax && ok && !Cfg::kDoubleS; ++j) {
           const int iv = 2 * j + 1, ik = 2 * j + 2;
           const int slot_v = iv % STAGES, slot_k = ik % STAGES;
           const bool next = j + 1 < nmax;
@@ -378,23 +420,23 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
           if (!wait_bar3(bv, pv, bp, pp, bk, pk, abort, p.timeout_ns)) { ok = false; break; }
           tc_fence_after_sync();
           if (j < n0) {
-            issue_pv(0, slot_v, j > 0);
+            issue_pv(0, slot_v, j > 0, 0);
             mma_commit(&bars->o_done[0]);
           }
           if (!kEarlyK && next) {
             if (!wait_bar(&bars->kv_full[slot_k], (ik / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
             tc_fence_after_sync();
           }
-          if (next && j + 1 < n0) { issue_s(0, slot_k); mma_commit(&bars->s_full[0]); }
+          if (next && j + 1 < n0) { issue_s(0, slot_k, 0); mma_commit(&bars->s_full[0]); }
           if (j < n1) {
             if (!wait_bar(&bars->p_ready[1], j & 1, abort, p.timeout_ns)) { ok = false; break; }
             tc_fence_after_sync();
-            issue_pv(1, slot_v, j > 0);
+            issue_pv(1, slot_v, j > 0, 1);
             mma_commit(&bars->o_done[1]);
           }
           mma_commit(&bars->kv_empty[slot_v]);
           if (next) {
-            if (j + 1 < n1) { issue_s(1, slot_k); mma_commit(&bars->s_full[1]); }
+            if (j + 1 < n1) { issue_s(1, slot_k, 1); mma_commit(&bars->s_full[1]); }
             mma_commit(&bars->kv_empty[slot_k]);
           }
         }
@@ -415,7 +457,7 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
     const int sub_row0 = q_row0 + sub * kRowsPerSub;
     const int qi = sub_row0 + row;                        // query index within (b, h)
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_bits + sub * 128;
+    const uint32_t tS0 = tmem + lane_bits + sub * 128;
     const uint32_t tO = tmem + lane_bits + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
     const float sl2 = p.scale_log2;
 
@@ -424,7 +466,11 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       // all lanes must agree before the warp-collective TMEM accesses
-      if (!__all_sync(0xffffffffu, wait_bar(&bars->s_full[sub], j & 1, abort, p.timeout_ns))) {
+      // S of this tile: the sub-tile's buffer, or buffer j % 2 when double-buffered
+      uint64_t* sbar = &bars->s_full[Cfg::kDoubleS ? (j & 1) : sub];
+      const uint32_t s_phase = Cfg::kDoubleS ? (j >> 1) & 1 : j & 1;
+      const uint32_t tS = Cfg::kDoubleS ? tS0 + (j & 1) * 128 : tS0;
+      if (!__all_sync(0xffffffffu, wait_bar(sbar, s_phase, abort, p.timeout_ns))) {
         ok = false;
         break;
       }
@@ -515,7 +561,7 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      bar_arrive(&bars->p_ready[sub]);
+      bar_arrive(&bars->p_ready[Cfg::kDoubleS ? (j & 1) : sub]);
       if (!ok) break;
     }
 
@@ -601,8 +647,9 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
           ok = __all_sync(0xffffffffu, ok);
         }
         if (store) *lse_out = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        // the stores must be complete before the CTA exits
-        if (leader) bulk_wait_all();
+        // The stores must have read the staged O before the CTA exits (its
+        // shared memory goes away); their global writes complete with the grid.
+        if (leader) bulk_wait_read();
       }
     }
     if (!ok) raise_abort(abort, p.status);

@@ -16,9 +16,11 @@ cudaError_t prepare_tc_d64_bf16();
 cudaError_t prepare_tc_d128_bf16();
 cudaError_t prepare_tc_d64_f16();
 cudaError_t prepare_tc_d128_f16();
+cudaError_t prepare_tc_d256_bf16();
+cudaError_t prepare_tc_d256_f16();
 cudaError_t prepare_simt();
 
-// subs: query sub-tiles of 128 rows per CTA (1 or 2).  mo: the map the epilogue stores O (or
+// subs: query sub-tiles of 128 rows per CTA (1 or 2; head dimension 256: 1).  mo: the map the epilogue stores O (or
 // the split-KV partial O) through.
 #define FA2_DECLARE_TC_LAUNCH(name)                                                          \
   cudaError_t name(int subs, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,      \
@@ -28,6 +30,8 @@ FA2_DECLARE_TC_LAUNCH(launch_tc_d64_bf16)
 FA2_DECLARE_TC_LAUNCH(launch_tc_d128_bf16)
 FA2_DECLARE_TC_LAUNCH(launch_tc_d64_f16)
 FA2_DECLARE_TC_LAUNCH(launch_tc_d128_f16)
+FA2_DECLARE_TC_LAUNCH(launch_tc_d256_bf16)
+FA2_DECLARE_TC_LAUNCH(launch_tc_d256_f16)
 #undef FA2_DECLARE_TC_LAUNCH
 cudaError_t launch_simt(int d, bool causal, const fa2dev::SimtParams& p, dim3 grid, cudaStream_t s);
 

@@ -73,10 +73,19 @@ WORKLOADS = [
 ]
 
 
+# Further measured shapes beyond the five: a long causal sequence at head
+# dimension 256 (the largest head size in the arithmetic-intensity table of
+# "Flash Attention 全解析(上)", section 1), with the same FLOP count as the
+# 16384-length d=128 case.
+EXTRA_WORKLOADS = [
+    Workload("b1_h16_n16384_d256_causal", 1, 16, 16384, 16384, 256, True, seed=6),
+]
+
+
 def workload(name_or_index) -> Workload:
     if isinstance(name_or_index, int):
         return WORKLOADS[name_or_index]
-    for w in WORKLOADS:
+    for w in WORKLOADS + EXTRA_WORKLOADS:
         if w.name == name_or_index:
             return w
     raise KeyError(name_or_index)

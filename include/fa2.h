@@ -53,7 +53,7 @@ typedef enum {
   FA2_ERR_NULL = 1,     /* a required pointer is NULL */
   FA2_ERR_ALIGN = 2,    /* Q/K/V/O not 16-byte aligned, or LSE not 4-byte aligned */
   FA2_ERR_SHAPE = 3,    /* negative size, Nk < 1 with rows to compute, or a size past the limits */
-  FA2_ERR_HEADDIM = 4,  /* d not supported (64 or 128) */
+  FA2_ERR_HEADDIM = 4,  /* d not supported (forward 64, 128 or 256; SIMT and backward 64 or 128) */
   FA2_ERR_LAUNCH = 5,   /* the CUDA launch or a CUDA call failed */
   FA2_ERR_TIMEOUT = 6,  /* a kernel gave up waiting on an internal barrier */
   FA2_ERR_SCALE = 7,    /* scale not finite and > 0 */
@@ -73,7 +73,8 @@ typedef enum { FA2_DTYPE_BF16 = 0, FA2_DTYPE_FP16 = 1, FA2_DTYPE_FP32 = 2 } fa2_
  *   O, LSE    device fp32 outputs
  *   B, H      batch and head counts (B*H <= 2^31-1)
  *   Nq, Nk    query and key lengths (may differ; Nk >= 1 when B*H*Nq > 0)
- *   d         head dimension, 64 or 128
+ *   d         head dimension, 64, 128 or 256 (256: one 128-row query tile per
+ *             CTA and one CTA per SM, the K/V tiles being 64 KB each)
  *   causal    nonzero: mask keys j > i
  *   scale     score scale, finite and > 0 (usually 1/sqrt(d))
  *   stream    CUDA stream (NULL = legacy default stream)
@@ -99,7 +100,8 @@ int fa2_forward_typed(const void *Q, const void *K, const void *V, void *O, floa
 /*
  * The same operation on the CUDA cores, fp32 arithmetic, one thread per query
  * row.  A plain second implementation used to cross-check fa2_forward on the
- * device; slow.  Same arguments, limits and errors, plus B*H <= 65535.
+ * device; slow.  Same arguments, limits and errors, plus B*H <= 65535 and
+ * d = 64 or 128 (256 returns FA2_ERR_HEADDIM).
  */
 int fa2_forward_simt(const void *Q, const void *K, const void *V, float *O, float *LSE, int B,
                      int H, int Nq, int Nk, int d, int causal, float scale, fa2_stream_t stream);
@@ -143,7 +145,7 @@ int fa2_forward_splitkv(const void *Q, const void *K, const void *V, float *O, f
  * gets O = 0 and LSE = -inf.
  *   O_parts    device fp32 [num_parts, rows, d], 16-byte aligned
  *   LSE_parts  device fp32 [num_parts, rows], 4-byte aligned
- *   num_parts  1..64;  rows >= 0 (0: nothing launched);  d: 64 or 128
+ *   num_parts  1..64;  rows >= 0 (0: nothing launched);  d: 64, 128 or 256
  *   O, LSE     device fp32 [rows, d] and [rows] outputs (must not overlap the parts)
  */
 int fa2_merge(const float *O_parts, const float *LSE_parts, int num_parts, long long rows, int d,
@@ -201,7 +203,8 @@ size_t fa2_backward_workspace_bytes(int B, int H, int Nq);
  *   workspace device scratch of fa2_backward_workspace_bytes(B, H, Nq) bytes
  *             or more, 256-byte aligned, owned by the caller; its contents
  *             on entry do not matter
- *   B, H, Nq, Nk, d, causal, scale, stream   as in fa2_forward
+ *   B, H, Nq, Nk, d, causal, scale, stream   as in fa2_forward, but d = 64
+ *             or 128 (256 returns FA2_ERR_HEADDIM)
  * Q, K, V, O, dO, dQ, dK and dV must be 16-byte aligned, LSE 4-byte aligned.
  * B*H == 0 is a valid empty problem.  Nq == 0 with Nk > 0 writes zeros to dK
  * and dV (no query sees any key); Q, K, V, O, dO, LSE, dQ and workspace may

@@ -72,10 +72,12 @@ def test_host_side_argument_errors(lib, fn):
     assert c(Nk=-1) == fa2.FA2_ERR_SHAPE
     assert c(Nk=0) == fa2.FA2_ERR_SHAPE
     assert c(B=1 << 16, H=1 << 16) == fa2.FA2_ERR_SHAPE
-    for d in (0, 32, 96, 256):
+    for d in (0, 32, 96, 192, 512):
         assert c(d=d) == fa2.FA2_ERR_HEADDIM
     for s in (0.0, -1.0, float("inf"), float("nan")):
         assert c(scale=s) == fa2.FA2_ERR_SCALE
+    # head dimension 256 passes the head-dimension check (the scale check comes next)
+    assert c(d=256, scale=0.0) == fa2.FA2_ERR_SCALE
     for name in ("Q", "K", "V", "O", "LSE"):
         assert c(**{name: None}) == fa2.FA2_ERR_NULL
     for name in ("Q", "K", "V", "O"):
@@ -116,7 +118,7 @@ def test_backward_host_side_argument_errors(lib):
     # sizes
     assert c(Nq=-1) == fa2.FA2_ERR_SHAPE
     assert c(Nk=0) == fa2.FA2_ERR_SHAPE
-    for d in (0, 32, 96, 256):
+    for d in (0, 32, 96, 256):   # the backward kernels cover 64 and 128
         assert c(d=d) == fa2.FA2_ERR_HEADDIM
     for s in (0.0, -1.0, float("inf"), float("nan")):
         assert c(scale=s) == fa2.FA2_ERR_SCALE
@@ -128,3 +130,12 @@ def test_backward_host_side_argument_errors(lib):
         assert c(**{name: 24}) == fa2.FA2_ERR_ALIGN
     assert c(LSE=18) == fa2.FA2_ERR_ALIGN
     assert c(ws=272) == fa2.FA2_ERR_ALIGN
+
+
+def test_splitkv_workspace_and_merge_head_dims(lib):
+    # O_part [S][rows][d] fp32 then LSE_part [S][rows], each rounded up to 256 bytes
+    assert fa2.fa2_splitkv_workspace_bytes(1, 2, 100, 256, 3) == 3 * 200 * 256 * 4 + 2560
+    assert fa2.fa2_splitkv_workspace_bytes(1, 2, 100, 96, 3) == 0
+    # merge: head dimension checked before the pointers
+    assert fa2.fa2_merge(None, None, 2, 8, 96, None, None, None) == fa2.FA2_ERR_HEADDIM
+    assert fa2.fa2_merge(None, None, 2, 8, 256, None, None, None) == fa2.FA2_ERR_NULL

@@ -36,7 +36,7 @@ CASES = [(1, 2, 1, 1), (1, 3, 130, 70), (2, 2, 257, 1000), (1, 2, 1000, 1000), (
 
 
 @pytest.mark.parametrize("in_name,out_name", [("fp16", "fp32"), ("fp16", "same"), ("bf16", "same")])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,H,Nq,Nk", CASES)
 def test_element_types(dev, in_name, out_name, d, causal, B, H, Nq, Nk):

@@ -116,7 +116,7 @@ def test_worked_example_blockwise_recurrence(oracle_mod):
 
 SHAPES = [
     (1, 1, 1, 1, 1), (1, 1, 5, 7, 4), (2, 3, 9, 9, 16), (1, 2, 17, 5, 8),
-    (1, 1, 33, 64, 64), (2, 1, 64, 33, 64), (1, 1, 20, 20, 128),
+    (1, 1, 33, 64, 64), (2, 1, 64, 33, 64), (1, 1, 20, 20, 128), (1, 2, 19, 23, 256),
 ]
 
 

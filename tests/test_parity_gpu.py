@@ -102,7 +102,7 @@ EDGE = [(1, 1), (2, 2), (1, 300), (63, 63), (64, 64), (65, 65), (127, 127), (128
         (100, 700), (700, 100), (129, 1), (5, 257), (513, 129)]
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("nq,nk", EDGE)
 def test_edge_sizes(dev, nq, nk, d, causal):
@@ -121,6 +121,30 @@ def test_peaky_scores_and_non_default_scale(dev):
         O, L = gpu_forward(dev, Q, K, V, causal, 0.3)
         Or, Lr = oracle.attention(*bits(Q, K, V), causal, 0.3)
         assert_close(O, L, Or, Lr, f"peaky causal={causal}")
+
+
+def test_head_dim_256_peaky_scores(dev):
+    """Head dimension 256 (one sub-tile per CTA, two S buffers in TMEM) with a
+    large score spread, so that the running-max correction of O runs while
+    the next tile's S is being computed."""
+    Q, K, V = inputs.make_qkv(1, 3, 900, 1300, 256, seed=78, qk_std=3.0)
+    for causal in (False, True):
+        O, L = gpu_forward(dev, Q, K, V, causal, 0.2)
+        Or, Lr = oracle.attention(*bits(Q, K, V), causal, 0.2)
+        assert_close(O, L, Or, Lr, f"d=256 peaky causal={causal}")
+
+
+def test_head_dim_256_long_sequence_sampled_rows(dev):
+    """A long causal problem at head dimension 256 (grid of several waves),
+    sampled rows against the oracle."""
+    B, H, N, d = 2, 8, 4096, 256
+    Q, K, V = inputs.make_qkv(B, H, N, N, d, seed=256)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    O, L = gpu_forward(dev, Q, K, V, True, scale)
+    rows = sample_rows(B, H, N, n_random=160, seed=256)
+    Or, Lr = oracle.attention_rows(*bits(Q, K, V), True, scale, rows)
+    idx = torch.as_tensor(rows, device=dev)
+    assert_close(O.reshape(-1, d)[idx], L.reshape(-1)[idx], Or, Lr, "d=256 N=4096 causal")
 
 
 def test_increasing_max_every_tile(dev):
@@ -221,7 +245,7 @@ TWO_SUBTILE_EDGE = [(1, 64, 1200, 1200), (1, 152, 257, 300), (2, 51, 513, 129), 
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("B,H,Nq,Nk", TWO_SUBTILE_EDGE)
 def test_edge_sizes_two_subtile_grid(dev, B, H, Nq, Nk, d, causal):
     assert (Nq + 255) // 256 * B * H >= 2 * torch.cuda.get_device_properties(0).multi_processor_count

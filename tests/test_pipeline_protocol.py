@@ -132,18 +132,21 @@ class Sim:
             op = self.mma_queue.pop(0)
         if op[0] == "mma" and op[2] is not None:
             kind, sub, j = op[2]
-            state = self.tmem_s[sub]
+            buf = self.s_buf(sub, j)
+            state = self.tmem_s[buf]
             if kind == "S":
-                # S_sub(j) overwrites P_sub(j-1): the PV that reads it must have run
-                if j > 0 and state != ("P-read", j - 1):
+                # S_sub(j) overwrites the P last written into its buffer: the
+                # PV that reads that P must have run
+                prev = j - self.s_reuse
+                if prev >= 0 and state != ("P-read", prev):
                     raise ProtocolError(f"S{sub}({j}) executes while TMEM holds {state}")
-                self.tmem_s[sub] = ("S", j)
+                self.tmem_s[buf] = ("S", j)
             else:
                 if state != ("P", j):
                     raise ProtocolError(f"PV{sub}({j}) executes while TMEM holds {state}")
                 if self.o_tiles[sub] != j - 1:
                     raise ProtocolError(f"PV{sub}({j}) accumulates onto O holding tile {self.o_tiles[sub]}")
-                self.tmem_s[sub] = ("P-read", j)
+                self.tmem_s[buf] = ("P-read", j)
                 self.o_tiles[sub] = j
         if op[0] == "commit":
             _, bar, release = op[:3]
@@ -153,6 +156,13 @@ class Sim:
                     raise ProtocolError(f"release of load {g}: slot {slot} holds {self.slot[slot]}")
                 self.slot[slot] = ("free", None)
             bar.arrive()
+
+    # S buffer of sub-tile `sub` at key tile j, and the tiles between two
+    # uses of one buffer: one buffer per sub-tile here.
+    s_reuse = 1
+
+    def s_buf(self, sub, j):
+        return sub
 
     # -------------------------------------------------------- roles
     def producer(self):
@@ -222,22 +232,32 @@ class Sim:
         while not self.drain.done(0):
             yield
 
+    def s_barrier(self, sub, j):
+        """(barrier, phase) announcing S_sub(j)."""
+        return self.s_full[sub], j
+
+    def p_barrier(self, sub, j):
+        """(barrier, phase) announcing P_sub(j)."""
+        return self.p_ready[sub], j
+
     def softmax(self, sub):
         n = self.n[sub]
         for j in range(n):
-            while not self.s_full[sub].done(j):
+            bar, ph = self.s_barrier(sub, j)
+            while not bar.done(ph):
                 yield
-            if self.tmem_s[sub] != ("S", j):
-                raise ProtocolError(f"softmax{sub}({j}) reads TMEM holding {self.tmem_s[sub]}")
+            buf = self.s_buf(sub, j)
+            if self.tmem_s[buf] != ("S", j):
+                raise ProtocolError(f"softmax{sub}({j}) reads TMEM holding {self.tmem_s[buf]}")
             yield
-            self.tmem_s[sub] = ("P", j)
+            self.tmem_s[buf] = ("P", j)
             if j > 0 and self.rng.random() < self.rescale_prob:
                 while not self.o_done[sub].done(j - 1):
                     yield
                 # the rescale reads and writes O: it must hold tiles 0..j-1 exactly
                 if self.o_tiles[sub] != j - 1:
                     raise ProtocolError(f"rescale at tile {j} sees O holding tile {self.o_tiles[sub]}")
-            self.p_ready[sub].arrive()
+            self.p_barrier(sub, j)[0].arrive()
         if n > 0:
             while not self.o_done[sub].done(n - 1):
                 yield
@@ -274,6 +294,77 @@ class Sim:
         for i, st in enumerate(self.slot):
             if st[0] == "loading":
                 raise ProtocolError(f"slot {i} still loading at exit")
+
+
+class DoubleSSim(Sim):
+    """One sub-tile with two S buffers in TMEM (head dimension 256): S(j+1)
+    is issued as soon as K(j+1) has landed, before P(j) V; S(j) and P(j) are
+    announced on s_full[j % 2] and p_ready[j % 2]."""
+    s_reuse = 2
+
+    def __init__(self, stages, n0, seed, single_p_ready=False, **kw):
+        super().__init__(stages, n0, 0, seed, **kw)
+        self.single_p_ready = single_p_ready
+
+    def s_buf(self, sub, j):
+        return j % 2
+
+    def s_barrier(self, sub, j):
+        return self.s_full[j % 2], j // 2
+
+    def p_barrier(self, sub, j):
+        if self.single_p_ready:
+            return self.p_ready[0], j
+        return self.p_ready[j % 2], j // 2
+
+    def issuer(self):
+        S = self.S
+        n0 = self.n[0]
+        while not self.q_full.done(0):
+            yield
+        while not self.slot_full[0].done(0):
+            yield
+        if n0 > 0:
+            self.mma([(0, 0)], ("S", 0, 0))
+            self.commit(self.s_full[0])
+        self.commit(self.slot_empty[0], release=(0, 0))
+        for j in range(n0):
+            gv, gk = 2 * j + 1, 2 * j + 2
+            if j + 1 < n0:
+                while not self.slot_full[gk % S].done(gk // S):
+                    yield
+                self.mma([(gk % S, gk)], ("S", 0, j + 1))
+                self.commit(self.s_full[(j + 1) % 2])
+                self.commit(self.slot_empty[gk % S], release=(gk % S, gk))
+            bar, ph = self.p_barrier(0, j)
+            while not (self.slot_full[gv % S].done(gv // S) and bar.done(ph)):
+                yield
+            self.mma([(gv % S, gv)], ("PV", 0, j))
+            self.commit(self.o_done[0])
+            self.commit(self.slot_empty[gv % S], release=(gv % S, gv))
+            yield
+        self.commit(self.drain)
+        while not self.drain.done(0):
+            yield
+
+
+@pytest.mark.parametrize("n0", list(range(1, 9)) + [17])
+def test_double_s_protocol_random_interleavings(n0):
+    for seed in range(60):
+        DoubleSSim(2, n0, seed).run()
+
+
+def test_model_catches_single_p_ready_with_double_s():
+    """With S double-buffered, the softmax can finish tile j + 1 before the
+    issuer has looked at P(j): a single p_ready barrier would then be two
+    phases ahead of the issuer's parity wait."""
+    failures = 0
+    for seed in range(300):
+        try:
+            DoubleSSim(2, 6, seed, single_p_ready=True, rescale_prob=0.0).run()
+        except ProtocolError:
+            failures += 1
+    assert failures > 0
 
 
 CASES = []

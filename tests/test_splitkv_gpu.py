@@ -54,6 +54,8 @@ CASES = [  # B, H, Nq, Nk, d, causal, splits
     (2, 2, 300, 5000, 128, False, 64),    # more splits requested than useful
     (1, 1, 128, 129, 128, False, 2),      # second range is a single key
     (1, 2, 256, 100, 64, True, 4),        # one key tile: falls back to one pass
+    (2, 2, 3, 5000, 256, False, 6),       # head dimension 256, decode-like
+    (1, 2, 700, 900, 256, True, 3),
 ]
 
 
