@@ -577,28 +577,39 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
       *lse_out = -INFINITY;
     }
     if (n_tiles > 0 && ok) {
+      // l == 0 only for a row whose every key in this range is masked
+      if (store) *lse_out = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       if (!__all_sync(0xffffffffu,
                       wait_bar(&bars->o_done[sub], (n_tiles - 1) & 1, abort, p.timeout_ns))) {
         ok = false;
       } else {
         tc_fence_after_sync();
-        // O / l is written into this sub-tile's Q buffer (every S MMA that
-        // read it has completed) as 128-byte-swizzled boxes, which one thread
-        // stores with TMA; rows past Nq fall outside the map and are dropped.
-        // fp32 O takes two rounds of D/2 columns (boxes of 32 columns), O in
-        // the input type one round (boxes of 64 columns).
-        // l == 0 only for a row whose every key in this range is masked
+        // O / l is written into shared memory as 128-byte-swizzled boxes,
+        // which one thread stores with TMA; rows past Nq fall outside the map
+        // and are dropped.  fp32 O takes two rounds of D/2 columns (boxes of
+        // 32 columns), O in the input type one round (boxes of 64 columns).
+        // Round 0 goes to this sub-tile's Q buffer (every S MMA that read it
+        // has completed).  Round 1 of the sub-tile(s) whose last P V is the
+        // CTA's last MMA goes to K/V ring slot `sub`, free once every MMA has
+        // completed (no load is in flight by then), so that both rounds are
+        // staged without waiting for the first stores; otherwise round 1
+        // reuses the Q buffer once the first stores have read it.
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        uint8_t* stage = sQ + sub * TILE;
-        const uint32_t stage_row = smem_addr(stage) + row * 128;
+        const bool use_ring = n_tiles == nmax;
         const int zrow = (p.num_splits > 1 ? split * p.BH : 0) + bh;
         const bool leader = (threadIdx.x & (kRowsPerSub - 1)) == 0;
         const int rounds = half_out ? 1 : 2;
         for (int r = 0; r < rounds && ok; ++r) {
-          if (r > 0 && !__all_sync(0xffffffffu, wait_bar(&bars->stage_free[sub], 0, abort, p.timeout_ns))) {
-            ok = false;
-            break;
+          if (r > 0) {
+            uint64_t* free_bar = use_ring ? &bars->mma_drain : &bars->stage_free[sub];
+            if (!__all_sync(0xffffffffu, wait_bar(free_bar, 0, abort, p.timeout_ns))) {
+              ok = false;
+              break;
+            }
+            if (use_ring) tc_fence_after_sync();
           }
+          uint8_t* stage = (r > 0 && use_ring ? sKV : sQ) + sub * TILE;
+          const uint32_t stage_row = smem_addr(stage) + row * 128;
 #pragma unroll
           for (int b = 0; b < D / 64; ++b) {
             const uint32_t box = stage_row + b * 16384;
@@ -638,7 +649,7 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
               for (int b = 0; b < D / 64; ++b)
                 tma_store_3d(&tm_o, stage + b * 16384, half_out ? 64 * b : r * (D / 2) + 32 * b, sub_row0, zrow);
               bulk_commit();
-              if (r + 1 < rounds) {
+              if (r + 1 < rounds && !use_ring) {
                 bulk_wait_read();
                 bar_arrive(&bars->stage_free[sub]);
               }
@@ -646,7 +657,6 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
           }
           ok = __all_sync(0xffffffffu, ok);
         }
-        if (store) *lse_out = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         // The stores must have read the staged O before the CTA exits (its
         // shared memory goes away); their global writes complete with the grid.
         if (leader) bulk_wait_read();

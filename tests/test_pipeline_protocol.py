@@ -157,6 +157,10 @@ class Sim:
                 self.slot[slot] = ("free", None)
             bar.arrive()
 
+    # The epilogue's wait for every MMA before it stages O in the ring (off
+    # only in the test that checks the model rejects its absence).
+    epilogue_waits_drain = True
+
     # S buffer of sub-tile `sub` at key tile j, and the tiles between two
     # uses of one buffer: one buffer per sub-tile here.
     s_reuse = 1
@@ -263,6 +267,16 @@ class Sim:
                 yield
             if self.o_tiles[sub] != n - 1:
                 raise ProtocolError(f"epilogue of sub-tile {sub} sees O holding tile {self.o_tiles[sub]}")
+            if n == self.nmax:
+                # the second epilogue round of a last-finishing sub-tile is
+                # staged in ring slot `sub` once every MMA has completed: no
+                # copy may still be writing the ring, no MMA still reading it
+                while self.epilogue_waits_drain and not self.drain.done(0):
+                    yield
+                if any(slot is not None for _, slot, _, _ in self.tma_inflight):
+                    raise ProtocolError("epilogue stages O in the ring while a K/V copy is in flight")
+                if any(op[0] == "mma" and op[1] for op in self.mma_queue):
+                    raise ProtocolError("epilogue stages O in the ring while an MMA may read it")
 
     # -------------------------------------------------------- scheduler
     def issuers(self):
@@ -362,6 +376,22 @@ def test_model_catches_single_p_ready_with_double_s():
     for seed in range(300):
         try:
             DoubleSSim(2, 6, seed, single_p_ready=True, rescale_prob=0.0).run()
+        except ProtocolError:
+            failures += 1
+    assert failures > 0
+
+
+def test_model_catches_ring_staging_without_drain():
+    """Staging O in a ring slot as soon as the sub-tile's own last P V is done
+    (without waiting for every MMA) races the other sub-tile's MMAs and the
+    last copies; the model must see it."""
+    class NoDrain(Sim):
+        epilogue_waits_drain = False
+
+    failures = 0
+    for seed in range(200):
+        try:
+            NoDrain(4, 5, 5, seed).run()
         except ProtocolError:
             failures += 1
     assert failures > 0
