@@ -154,6 +154,17 @@ bool encode_map_out(CUtensorMap* map, const void* base, int d, int Nq, long long
   return r == CUDA_SUCCESS;
 }
 
+// Multiplier and shift of fa2dev::fast_div for a divisor d >= 1.
+fa2dev::FastDiv make_fast_div(int d) {
+  int l = 0;
+  while ((1LL << l) < d) ++l;
+  const unsigned long long two = 1ULL << (31 + l);
+  fa2dev::FastDiv f;
+  f.m = static_cast<uint32_t>((two + static_cast<unsigned long long>(d) - 1) / static_cast<unsigned long long>(d));
+  f.s = 31 + l;
+  return f;
+}
+
 // Head dimensions of the tensor-core forward kernels (and of the merge).
 bool forward_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
@@ -249,6 +260,9 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   p.LSE_part = LSE_part;
   p.o_half = o_half ? 1 : 0;
   p.item_group = item_group(pr, splits);
+  p.div_per_group = make_fast_div(static_cast<int>(p.item_group * blocks));
+  p.div_group = make_fast_div(p.item_group);
+  p.div_splits = make_fast_div(splits);
   p.wave = sm_count() * (subs == 2 || d == 256 ? 1 : 2);
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
     return FA2_ERR_LAUNCH;

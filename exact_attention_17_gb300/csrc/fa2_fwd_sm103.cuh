@@ -54,6 +54,21 @@ namespace fa2dev {
 // Error bits OR-ed into the library's device status word.
 constexpr int kDevErrTimeout = 1;
 
+// Division by a divisor that is fixed for a launch, as one widening multiply
+// and a shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): for 0 <= n < 2^31 and d >= 1, with l = ceil(log2 d),
+// m = ceil(2^(31+l) / d) < 2^32 and s = 31 + l, floor(n / d) = (n m) >> s.
+// A division by a run-time divisor costs about two hundred cycles, and the
+// work-item decode at CTA start had a chain of three.
+struct FastDiv {
+  uint32_t m;
+  int s;
+};
+
+__host__ __device__ __forceinline__ int fast_div(int n, const FastDiv& f) {
+  return static_cast<int>((static_cast<unsigned long long>(static_cast<uint32_t>(n)) * f.m) >> f.s);
+}
+
 struct FwdParams {
   float* O;        // [BH, Nq, D] fp32 (num_splits == 1)
   float* LSE;      // [BH, Nq]    fp32 (num_splits == 1)
@@ -81,6 +96,9 @@ struct FwdParams {
   // within a group CTAs run query block by query block across the group's
   // items, heaviest causal blocks first.
   int item_group;
+  FastDiv div_per_group;  // by item_group * q_blocks
+  FastDiv div_group;      // by item_group
+  FastDiv div_splits;     // by num_splits
 };
 
 constexpr int kRowsPerSub = 128;   // tcgen05 M
@@ -203,13 +221,14 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
   const int U = p.q_blocks;
   const int items = p.BH * p.num_splits;
   const int per_group = p.item_group * U;
-  const int group = blockIdx.x / per_group;
+  const int group = fast_div(static_cast<int>(blockIdx.x), p.div_per_group);
   const int in_group = blockIdx.x - group * per_group;
   const int g0 = group * p.item_group;
   const int g_items = min(p.item_group, items - g0);
-  const int u_rank = in_group / g_items;
+  // only the last group can be short
+  const int u_rank = g_items == p.item_group ? fast_div(in_group, p.div_group) : in_group / g_items;
   const int item = g0 + (in_group - u_rank * g_items);
-  const int bh = item / p.num_splits;
+  const int bh = fast_div(item, p.div_splits);
   const int split = item - bh * p.num_splits;
   const int u = CAUSAL ? U - 1 - u_rank : u_rank;
   const int all_tiles = (p.Nk + kKeysPerTile - 1) / kKeysPerTile;

@@ -139,3 +139,32 @@ def test_splitkv_workspace_and_merge_head_dims(lib):
     # merge: head dimension checked before the pointers
     assert fa2.fa2_merge(None, None, 2, 8, 96, None, None, None) == fa2.FA2_ERR_HEADDIM
     assert fa2.fa2_merge(None, None, 2, 8, 256, None, None, None) == fa2.FA2_ERR_NULL
+
+
+def test_fast_division_method():
+    """The multiply-and-shift division the forward kernel uses to decode its
+    work item (divisors fixed per launch): with l = ceil(log2 d),
+    m = ceil(2^(31+l) / d) and s = 31 + l, (n m) >> s == n // d for every
+    0 <= n < 2^31 (Granlund and Montgomery 1994).  Checked on the divisors
+    where the rounding excess is largest and on the numerators nearest to a
+    multiple of d and to 2^31."""
+    import random
+
+    def magic(d):
+        l = (d - 1).bit_length()
+        m = -(-(1 << (31 + l)) // d)
+        assert m < 1 << 32
+        return m, 31 + l
+
+    rng = random.Random(7)
+    divisors = list(range(1, 600)) + [2 ** k + e for k in range(1, 31) for e in (-1, 0, 1)
+                                      if 1 <= 2 ** k + e < 2 ** 31]
+    divisors += [rng.randrange(1, 2 ** 31) for _ in range(300)] + [2 ** 31 - 1]
+    for d in divisors:
+        m, s = magic(d)
+        ns = {0, 1, d - 1, d, d + 1, 2 ** 31 - 1, 2 ** 31 - 2}
+        top = (2 ** 31 - 1) // d * d
+        ns |= {top - 1, top, top + d - 1} | {rng.randrange(0, 2 ** 31) for _ in range(40)}
+        for n in ns:
+            if 0 <= n < 2 ** 31:
+                assert (n * m) >> s == n // d, (n, d)

@@ -403,6 +403,7 @@ for stages in (2, 4, 5, 8):
         CASES.append((stages, nmax, nmax))          # non-causal: both sub-tiles, same range
         CASES.append((stages, nmax - 1, nmax) if nmax > 1 else (stages, 1, 1))  # causal pair
         CASES.append((stages, nmax, 0))             # second sub-tile past the end
+    CASES.append((stages, 0, 1))   # causal key range that only the second sub-tile reaches
 
 
 @pytest.mark.parametrize("stages,n0,n1", CASES)
