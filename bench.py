@@ -51,6 +51,11 @@ KERNEL_SOURCES = ["exact_attention_17_gb300/csrc/fa2_fwd_sm103.cuh",
                   "exact_attention_17_gb300/csrc/fa2_tc_d128_bf16.cu"]
 
 
+def fwd_kernel_sources(d: int, fp16: bool = False):
+    """Sources of the forward kernel a workload runs (head dimension, element type)."""
+    return KERNEL_SOURCES[:2] + [f"exact_attention_17_gb300/csrc/fa2_tc_d{d}_{'f16' if fp16 else 'bf16'}.cu"]
+
+
 def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
     for rel in sources or KERNEL_SOURCES:
@@ -495,7 +500,7 @@ def main():
     algo_bytes = algorithmic_bytes(w, 2 if args.out_dtype == "same" else 4)
     balance = peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
     hbm_bound = w.flops / algo_bytes < balance
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name, fwd_kernel_sources(w.d, args.dtype == "fp16"))
 
     cpu = None
     if args.cpu_baseline_s > 0:
