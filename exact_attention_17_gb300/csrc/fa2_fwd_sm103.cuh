@@ -140,6 +140,14 @@ struct FwdConfig {
   // buffer while the softmax of the current one runs.  Otherwise one per
   // sub-tile, and S of the next tile overwrites P once P V is issued.
   static constexpr bool kDoubleS = D == 256;
+  // K/V ring slots released by a softmax thread instead of MMA commits:
+  // the completion of S_r(j) (r: the sub-tile that visits every key tile)
+  // implies that every MMA reading K_j and V_(j-1) has completed, and a
+  // commit costs the issuing thread time that idles the tensor pipe.  With a
+  // two-slot ring the V slot must be released as soon as P V completes, and
+  // the double-buffered issue order (S(j+1) before P(j) V) does not give the
+  // implication, so those keep the commits.
+  static constexpr bool kSoftmaxRelease = !kDoubleS && kStages >= 4;
   // TMEM columns: S buffers (128 fp32 columns each), then O of each sub-tile (D).
   static constexpr uint32_t kColsO0 = (kDoubleS ? 2 : SUBS) * 128;
   static constexpr uint32_t kColsO1 = kColsO0 + D;
@@ -388,7 +396,7 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
           tc_fence_after_sync();
           if (n0 > 0) { issue_s(0, 0, 0); mma_commit(&bars->s_full[0]); }
           if (n1 > 0) { issue_s(1, 0, 1); mma_commit(&bars->s_full[1]); }
-          mma_commit(&bars->kv_empty[0]);
+          if (!Cfg::kSoftmaxRelease) mma_commit(&bars->kv_empty[0]);
         }
         if constexpr (Cfg::kDoubleS) {
           // One sub-tile, S double-buffered: S(j+1) goes to the tensor pipe as
@@ -453,10 +461,10 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
             issue_pv(1, slot_v, j > 0, 1);
             mma_commit(&bars->o_done[1]);
           }
-          mma_commit(&bars->kv_empty[slot_v]);
+          if (!Cfg::kSoftmaxRelease) mma_commit(&bars->kv_empty[slot_v]);
           if (next) {
             if (j + 1 < n1) { issue_s(1, slot_k, 1); mma_commit(&bars->s_full[1]); }
-            mma_commit(&bars->kv_empty[slot_k]);
+            if (!Cfg::kSoftmaxRelease) mma_commit(&bars->kv_empty[slot_k]);
           }
         }
         if (!ok) raise_abort(abort, p.status);
@@ -480,6 +488,10 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
     const uint32_t tO = tmem + lane_bits + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
     const float sl2 = p.scale_log2;
 
+    // One thread of the sub-tile that visits every key tile of the range
+    // (the second, unless it has no rows) releases the K/V ring slots.
+    const bool releaser = (threadIdx.x & (kRowsPerSub - 1)) == 0 && n_tiles == nmax &&
+                          (sub == SUBS - 1 || n1 == 0);
     float m = -INFINITY;  // running max (log2 domain) used as the exponent offset
     float l = 0.f;        // running sum of 2^(t - m)
     bool ok = true;
@@ -494,6 +506,11 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         break;
       }
       tc_fence_after_sync();
+      if (Cfg::kSoftmaxRelease && releaser) {
+        // S_sub(j) complete: K_j and V_(j-1) have no reader left
+        if (j > 0) bar_arrive(&bars->kv_empty[(2 * j - 1) % STAGES]);
+        bar_arrive(&bars->kv_empty[(2 * j) % STAGES]);
+      }
       uint32_t s[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);

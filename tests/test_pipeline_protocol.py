@@ -130,6 +130,11 @@ class Sim:
             self.mma_queue.remove(op)
         else:
             op = self.mma_queue.pop(0)
+        if op[0] == "mma":
+            # the operands must still be in place when the MMA executes
+            for slot, g in op[1]:
+                if self.slot[slot] != ("ready", g):
+                    raise ProtocolError(f"MMA reading load {g} executes while slot {slot} holds {self.slot[slot]}")
         if op[0] == "mma" and op[2] is not None:
             kind, sub, j = op[2]
             buf = self.s_buf(sub, j)
@@ -160,6 +165,20 @@ class Sim:
     # The epilogue's wait for every MMA before it stages O in the ring (off
     # only in the test that checks the model rejects its absence).
     epilogue_waits_drain = True
+
+    # Ring slots released by a softmax thread of the sub-tile that visits
+    # every key tile, on seeing S of tile j complete (K_j and V_(j-1) have
+    # no reader left), instead of by MMA commits; rings of four or more slots.
+    @property
+    def softmax_release(self):
+        return self.S >= 4
+
+    def release(self, g):
+        slot = g % self.S
+        if self.slot[slot] != ("ready", g):
+            raise ProtocolError(f"release of load {g}: slot {slot} holds {self.slot[slot]}")
+        self.slot[slot] = ("free", None)
+        self.slot_empty[slot].arrive()
 
     # S buffer of sub-tile `sub` at key tile j, and the tiles between two
     # uses of one buffer: one buffer per sub-tile here.
@@ -204,7 +223,8 @@ class Sim:
             issue_s(0, 0)
         if n1 > 0:
             issue_s(1, 0)
-        self.commit(self.slot_empty[0], release=(0, 0))
+        if not self.softmax_release:
+            self.commit(self.slot_empty[0], release=(0, 0))
         for j in range(nmax):
             gv, gk = 2 * j + 1, 2 * j + 2
             nxt = j + 1 < nmax
@@ -226,11 +246,13 @@ class Sim:
                 while not self.p_ready[1].done(j):
                     yield
                 issue_pv(1, gv)
-            self.commit(self.slot_empty[gv % S], release=(gv % S, gv))
+            if not self.softmax_release:
+                self.commit(self.slot_empty[gv % S], release=(gv % S, gv))
             if nxt:
                 if j + 1 < n1:
                     issue_s(1, gk)
-                self.commit(self.slot_empty[gk % S], release=(gk % S, gk))
+                if not self.softmax_release:
+                    self.commit(self.slot_empty[gk % S], release=(gk % S, gk))
             yield
         self.commit(self.drain)
         while not self.drain.done(0):
@@ -246,10 +268,15 @@ class Sim:
 
     def softmax(self, sub):
         n = self.n[sub]
+        releaser = n == self.nmax and (sub == 1 or self.n[1] == 0)
         for j in range(n):
             bar, ph = self.s_barrier(sub, j)
             while not bar.done(ph):
                 yield
+            if self.softmax_release and releaser:
+                if j > 0:
+                    self.release(2 * j - 1)
+                self.release(2 * j)
             buf = self.s_buf(sub, j)
             if self.tmem_s[buf] != ("S", j):
                 raise ProtocolError(f"softmax{sub}({j}) reads TMEM holding {self.tmem_s[buf]}")
@@ -315,6 +342,7 @@ class DoubleSSim(Sim):
     is issued as soon as K(j+1) has landed, before P(j) V; S(j) and P(j) are
     announced on s_full[j % 2] and p_ready[j % 2]."""
     s_reuse = 2
+    softmax_release = False
 
     def __init__(self, stages, n0, seed, single_p_ready=False, **kw):
         super().__init__(stages, n0, 0, seed, **kw)
@@ -397,6 +425,39 @@ def test_model_catches_ring_staging_without_drain():
     assert failures > 0
 
 
+def test_model_catches_release_by_the_wrong_sub_tile():
+    """Under the causal mask the first sub-tile sees S_0(j) complete before
+    P_1(j-1) V has read V_(j-1): the slots must be released by the sub-tile
+    that visits every key tile, not by the first one."""
+    class WrongReleaser(Sim):
+        def softmax(self, sub):
+            n = self.n[sub]
+            for j in range(n):
+                bar, ph = self.s_barrier(sub, j)
+                while not bar.done(ph):
+                    yield
+                if sub == 0:
+                    if j > 0:
+                        self.release(2 * j - 1)
+                    self.release(2 * j)
+                if self.tmem_s[sub] != ("S", j):
+                    raise ProtocolError(f"softmax{sub}({j}) reads TMEM holding {self.tmem_s[sub]}")
+                yield
+                self.tmem_s[sub] = ("P", j)
+                self.p_ready[sub].arrive()
+            if n > 0:
+                while not self.o_done[sub].done(n - 1):
+                    yield
+
+    failures = 0
+    for seed in range(300):
+        try:
+            WrongReleaser(4, 5, 6, seed).run()
+        except ProtocolError:
+            failures += 1
+    assert failures > 0
+
+
 CASES = []
 for stages in (2, 4, 5, 8):
     for nmax in list(range(1, 11)) + [17]:
@@ -420,6 +481,8 @@ def test_model_catches_early_rearm():
     the model must reject it."""
 
     class GroupedSim(Sim):
+        softmax_release = False
+
         def producer(self):
             S, NG, nmax = self.S, self.NG, self.nmax
             self.q_full.arrive(tx_bytes=self.TILE)
