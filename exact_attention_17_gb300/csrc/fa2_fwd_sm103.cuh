@@ -148,6 +148,10 @@ struct FwdConfig {
   // the double-buffered issue order (S(j+1) before P(j) V) does not give the
   // implication, so those keep the commits.
   static constexpr bool kSoftmaxRelease = !kDoubleS && kStages >= 4;
+  // O of a sub-tile announced complete only after its last P V: in the
+  // single-buffered issue order S(j+1) follows P(j) V, so the softmax's wait
+  // for S(j+1) already orders its rescale of O after P(j) V.
+  static constexpr bool kOutDoneLast = !kDoubleS;
   // TMEM columns: S buffers (128 fp32 columns each), then O of each sub-tile (D).
   static constexpr uint32_t kColsO0 = (kDoubleS ? 2 : SUBS) * 128;
   static constexpr uint32_t kColsO1 = kColsO0 + D;
@@ -448,7 +452,7 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
           tc_fence_after_sync();
           if (j < n0) {
             issue_pv(0, slot_v, j > 0, 0);
-            mma_commit(&bars->o_done[0]);
+            if (!Cfg::kOutDoneLast || j + 1 == n0) mma_commit(&bars->o_done[0]);
           }
           if (!kEarlyK && next) {
             if (!wait_bar(&bars->kv_full[slot_k], (ik / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
             if (!wait_bar(&bars->p_ready[1], j & 1, abort, p.timeout_ns)) { ok = false; break; }
             tc_fence_after_sync();
             issue_pv(1, slot_v, j > 0, 1);
-            mma_commit(&bars->o_done[1]);
+            if (!Cfg::kOutDoneLast || j + 1 == n1) mma_commit(&bars->o_done[1]);
           }
           if (!Cfg::kSoftmaxRelease) mma_commit(&bars->kv_empty[slot_v]);
           if (next) {
@@ -578,8 +582,10 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
       tmem_st32(tS + 32, pk[1]);
 
       // correction of the running output when some row of this warp moved its offset
+      // (single-buffered order: the wait for S(j) above already follows P(j-1) V)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!__all_sync(0xffffffffu, wait_bar(&bars->o_done[sub], (j - 1) & 1, abort, p.timeout_ns))) {
+        if (!Cfg::kOutDoneLast &&
+            !__all_sync(0xffffffffu, wait_bar(&bars->o_done[sub], (j - 1) & 1, abort, p.timeout_ns))) {
           ok = false;
         }
         else {
@@ -616,7 +622,8 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
       // l == 0 only for a row whose every key in this range is masked
       if (store) *lse_out = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       if (!__all_sync(0xffffffffu,
-                      wait_bar(&bars->o_done[sub], (n_tiles - 1) & 1, abort, p.timeout_ns))) {
+                      wait_bar(&bars->o_done[sub], Cfg::kOutDoneLast ? 0u : (n_tiles - 1) & 1, abort,
+                               p.timeout_ns))) {
         ok = false;
       } else {
         tc_fence_after_sync();

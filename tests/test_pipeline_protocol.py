@@ -180,6 +180,13 @@ class Sim:
         self.slot[slot] = ("free", None)
         self.slot_empty[slot].arrive()
 
+    # O of a sub-tile is announced (o_done) only after its last P V.
+    out_done_last = True
+
+    def o_done_phase(self, n):
+        """Phase of o_done that announces the last P V of an n-tile sub-tile."""
+        return 0 if self.out_done_last else n - 1
+
     # S buffer of sub-tile `sub` at key tile j, and the tiles between two
     # uses of one buffer: one buffer per sub-tile here.
     s_reuse = 1
@@ -213,7 +220,8 @@ class Sim:
 
         def issue_pv(sub, g):
             self.mma([(g % S, g)], ("PV", sub, g // 2))
-            self.commit(self.o_done[sub])
+            if not self.out_done_last or g // 2 == self.n[sub] - 1:
+                self.commit(self.o_done[sub])
 
         while not self.q_full.done(0):
             yield
@@ -283,14 +291,16 @@ class Sim:
             yield
             self.tmem_s[buf] = ("P", j)
             if j > 0 and self.rng.random() < self.rescale_prob:
-                while not self.o_done[sub].done(j - 1):
+                # (with O announced only at the end, the wait for S(j) above
+                # must already order the rescale after P(j-1) V)
+                while not self.out_done_last and not self.o_done[sub].done(j - 1):
                     yield
                 # the rescale reads and writes O: it must hold tiles 0..j-1 exactly
                 if self.o_tiles[sub] != j - 1:
                     raise ProtocolError(f"rescale at tile {j} sees O holding tile {self.o_tiles[sub]}")
             self.p_barrier(sub, j)[0].arrive()
         if n > 0:
-            while not self.o_done[sub].done(n - 1):
+            while not self.o_done[sub].done(self.o_done_phase(n)):
                 yield
             if self.o_tiles[sub] != n - 1:
                 raise ProtocolError(f"epilogue of sub-tile {sub} sees O holding tile {self.o_tiles[sub]}")
@@ -343,6 +353,7 @@ class DoubleSSim(Sim):
     announced on s_full[j % 2] and p_ready[j % 2]."""
     s_reuse = 2
     softmax_release = False
+    out_done_last = False
 
     def __init__(self, stages, n0, seed, single_p_ready=False, **kw):
         super().__init__(stages, n0, 0, seed, **kw)
@@ -446,13 +457,57 @@ def test_model_catches_release_by_the_wrong_sub_tile():
                 self.tmem_s[sub] = ("P", j)
                 self.p_ready[sub].arrive()
             if n > 0:
-                while not self.o_done[sub].done(n - 1):
+                while not self.o_done[sub].done(self.o_done_phase(n)):
                     yield
 
     failures = 0
     for seed in range(300):
         try:
             WrongReleaser(4, 5, 6, seed).run()
+        except ProtocolError:
+            failures += 1
+    assert failures > 0
+
+
+def test_model_catches_rescale_before_pv_when_s_comes_first():
+    """Without per-tile o_done the rescale relies on S(j) being issued after
+    P(j-1) V; in the double-buffered order (S(j+1) ahead of P(j) V) that does
+    not hold, and the model must see the rescale racing P V."""
+    class DoubleNoDone(DoubleSSim):
+        out_done_last = True
+
+        def issuer(self):
+            S = self.S
+            n0 = self.n[0]
+            while not (self.q_full.done(0) and self.slot_full[0].done(0)):
+                yield
+            self.mma([(0, 0)], ("S", 0, 0))
+            self.commit(self.s_full[0])
+            self.commit(self.slot_empty[0], release=(0, 0))
+            for j in range(n0):
+                gv, gk = 2 * j + 1, 2 * j + 2
+                if j + 1 < n0:
+                    while not self.slot_full[gk % S].done(gk // S):
+                        yield
+                    self.mma([(gk % S, gk)], ("S", 0, j + 1))
+                    self.commit(self.s_full[(j + 1) % 2])
+                    self.commit(self.slot_empty[gk % S], release=(gk % S, gk))
+                bar, ph = self.p_barrier(0, j)
+                while not (self.slot_full[gv % S].done(gv // S) and bar.done(ph)):
+                    yield
+                self.mma([(gv % S, gv)], ("PV", 0, j))
+                if j == n0 - 1:
+                    self.commit(self.o_done[0])
+                self.commit(self.slot_empty[gv % S], release=(gv % S, gv))
+                yield
+            self.commit(self.drain)
+            while not self.drain.done(0):
+                yield
+
+    failures = 0
+    for seed in range(300):
+        try:
+            DoubleNoDone(2, 6, seed, rescale_prob=0.5).run()
         except ProtocolError:
             failures += 1
     assert failures > 0
@@ -482,6 +537,7 @@ def test_model_catches_early_rearm():
 
     class GroupedSim(Sim):
         softmax_release = False
+        out_done_last = False
 
         def producer(self):
             S, NG, nmax = self.S, self.NG, self.nmax
