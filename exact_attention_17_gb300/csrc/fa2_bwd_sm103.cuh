@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (int t = 0; t < n_tiles && ok; ++t) {
           const int slot = t % STAGES;
-          const int round = t / STAGES;
-          if (round > 0 && !wait_bar(&bars->q_empty[slot], (round - 1) & 1, abort, p.timeout_ns)) {
+          const int lap = t / STAGES;   // laps of the ring completed
+          if (lap > 0 && !wait_bar(&bars->q_empty[slot], (lap - 1) & 1, abort, p.timeout_ns)) {
             raise_abort(abort, p.status);
             ok = false;
             break;

@@ -331,8 +331,8 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         for (int j = primed / 2; j < nmax && ok; ++j) {
           for (int kind = (primed & 1) && j == primed / 2 ? 1 : 0; kind < 2; ++kind) {
             const int slot = issued % STAGES;
-            const int round = issued / STAGES;
-            if (round > 0 && !wait_bar(&bars->kv_empty[slot], (round - 1) & 1, abort, p.timeout_ns)) {
+            const int lap = issued / STAGES;   // laps of the ring completed
+            if (lap > 0 && !wait_bar(&bars->kv_empty[slot], (lap - 1) & 1, abort, p.timeout_ns)) {
               raise_abort(abort, p.status);
               ok = false;
               break;
@@ -629,20 +629,20 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         tc_fence_after_sync();
         // O / l is written into shared memory as 128-byte-swizzled boxes,
         // which one thread stores with TMA; rows past Nq fall outside the map
-        // and are dropped.  fp32 O takes two rounds of D/2 columns (boxes of
-        // 32 columns), O in the input type one round (boxes of 64 columns).
-        // Round 0 goes to this sub-tile's Q buffer (every S MMA that read it
-        // has completed).  Round 1 of the sub-tile(s) whose last P V is the
-        // CTA's last MMA goes to K/V ring slot `sub`, free once every MMA has
-        // completed (no load is in flight by then), so that both rounds are
-        // staged without waiting for the first stores; otherwise round 1
-        // reuses the Q buffer once the first stores have read it.
+        // and are dropped.  fp32 O is staged in two column halves of D/2
+        // (boxes of 32 columns), O in the input type all at once (boxes of 64
+        // columns).  The first half goes to this sub-tile's Q buffer (every S
+        // MMA that read it has completed).  The second half of the sub-tile(s)
+        // whose last P V is the CTA's last MMA goes to K/V ring slot `sub`,
+        // free once every MMA has completed (no load is in flight by then),
+        // so that both halves are staged without waiting for the first
+        // stores; otherwise it reuses the Q buffer once those have read it.
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const bool use_ring = n_tiles == nmax;
         const int zrow = (p.num_splits > 1 ? split * p.BH : 0) + bh;
         const bool leader = (threadIdx.x & (kRowsPerSub - 1)) == 0;
-        const int rounds = half_out ? 1 : 2;
-        for (int r = 0; r < rounds && ok; ++r) {
+        const int parts = half_out ? 1 : 2;   // column halves staged one after the other
+        for (int r = 0; r < parts && ok; ++r) {
           if (r > 0) {
             uint64_t* free_bar = use_ring ? &bars->mma_drain : &bars->stage_free[sub];
             if (!__all_sync(0xffffffffu, wait_bar(free_bar, 0, abort, p.timeout_ns))) {
@@ -692,7 +692,7 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
               for (int b = 0; b < D / 64; ++b)
                 tma_store_3d(&tm_o, stage + b * 16384, half_out ? 64 * b : r * (D / 2) + 32 * b, sub_row0, zrow);
               bulk_commit();
-              if (r + 1 < rounds && !use_ring) {
+              if (r + 1 < parts && !use_ring) {
                 bulk_wait_read();
                 bar_arrive(&bars->stage_free[sub]);
               }
