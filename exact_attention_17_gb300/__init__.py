@@ -46,6 +46,7 @@ SIGNATURES = {
     "fa2_backward": (_I, [_P] * 9 + [_I] * 6 + [ctypes.c_float, _P, _Z, _P]),
     "fa2_status_string": (ctypes.c_char_p, [_I]),
     "fa2_device_status": (_I, [_P, _I]),
+    "fa2_check_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
 }
 
 _lib = None
@@ -131,6 +132,11 @@ def fa2_status_string(status: int) -> str:
 
 def fa2_device_status(stream=None, reset: bool = False) -> int:
     return library().fa2_device_status(stream, int(bool(reset)))
+
+
+def fa2_check_wait_timeout(timeout_ns: int, stream=None) -> int:
+    """Raw C call: one bounded wait on a barrier nothing completes (see fa2.h)."""
+    return library().fa2_check_wait_timeout(int(timeout_ns), stream)
 
 
 def _stream_handle(stream):

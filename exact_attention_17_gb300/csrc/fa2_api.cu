@@ -519,6 +519,34 @@ extern "C" const char* fa2_status_string(int status) {
   }
 }
 
+namespace fa2dev {
+
+// One thread waits on an mbarrier that nothing completes, with the bounded
+// wait of the pipeline kernels, and records the timeout as they do.
+__global__ void fa2_wait_check_kernel(int* status, unsigned long long timeout_ns) {
+  __shared__ alignas(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    bar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    if (!wait_bar(&bar, 0, &abort_flag, timeout_ns)) atomicOr(status, kDevErrTimeout);
+  }
+}
+
+}  // namespace fa2dev
+
+extern "C" int fa2_check_wait_timeout(unsigned long long timeout_ns, fa2_stream_t stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return FA2_ERR_SHAPE;
+  const int rc = device_ready();
+  if (rc != FA2_OK) return rc;
+  int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_device_status) != cudaSuccess)
+    return FA2_ERR_LAUNCH;
+  fa2dev::fa2_wait_check_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, timeout_ns);
+  return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
+}
+
 extern "C" int fa2_device_status(fa2_stream_t stream, int reset) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA2_ERR_LAUNCH;
   int v = 0;

@@ -229,6 +229,17 @@ const char *fa2_status_string(int status);
  */
 int fa2_device_status(fa2_stream_t stream, int reset);
 
+/*
+ * Check of the failure path every pipeline wait has: launches one CTA whose
+ * thread waits, with the same bounded wait the kernels use, on an internal
+ * barrier that nothing completes.  The wait gives up after timeout_ns of
+ * wall time (1e3 <= timeout_ns <= 1e10, else FA2_ERR_SHAPE) and the kernel
+ * sets the device status word and returns, so that fa2_device_status then
+ * reports FA2_ERR_TIMEOUT and the context stays usable.  Asynchronous on
+ * `stream`; returns FA2_OK once launched.
+ */
+int fa2_check_wait_timeout(unsigned long long timeout_ns, fa2_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

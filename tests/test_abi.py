@@ -168,3 +168,8 @@ def test_fast_division_method():
         for n in ns:
             if 0 <= n < 2 ** 31:
                 assert (n * m) >> s == n // d, (n, d)
+
+
+def test_wait_check_rejects_out_of_range_limits_on_the_host(lib):
+    for t in (0, 999, 10_000_000_001):
+        assert fa2.fa2_check_wait_timeout(t) == fa2.FA2_ERR_SHAPE
