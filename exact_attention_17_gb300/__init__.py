@@ -44,6 +44,7 @@ SIGNATURES = {
     "fa2_forward_splitkv_static": (_I, _FORWARD_ARGS[:-1] + [_I, _P]),
     "fa2_backward_workspace_bytes": (_Z, [_I, _I, _I]),
     "fa2_backward": (_I, [_P] * 9 + [_I] * 6 + [ctypes.c_float, _P, _Z, _P]),
+    "fa2_backward_typed": (_I, [_P] * 9 + [_I] * 6 + [ctypes.c_float, _I, _P, _Z, _P]),
     "fa2_status_string": (ctypes.c_char_p, [_I]),
     "fa2_device_status": (_I, [_P, _I]),
     "fa2_check_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
@@ -124,6 +125,14 @@ def fa2_backward(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale
     """Raw C call of the backward pass (caller-provided device workspace)."""
     return library().fa2_backward(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d,
                                   int(bool(causal)), scale, workspace, workspace_size, stream)
+
+
+def fa2_backward_typed(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, qkv_dtype,
+                       workspace, workspace_size, stream) -> int:
+    """Raw C call of the backward pass with bf16 or fp16 Q, K, V and dO."""
+    return library().fa2_backward_typed(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d,
+                                        int(bool(causal)), scale, qkv_dtype, workspace, workspace_size,
+                                        stream)
 
 
 def fa2_status_string(status: int) -> str:
@@ -241,17 +250,20 @@ def merge(o_parts, lse_parts, out=None, lse=None, stream=None):
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, dq=None,
              dk=None, dv=None, workspace=None, stream=None):
-    """Attention backward on torch CUDA tensors (fa2_backward).
+    """Attention backward on torch CUDA tensors (fa2_backward_typed).
 
-    q, do: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; o fp32 [B,H,Nq,d] and lse
-    fp32 [B,H,Nq] as returned by ``forward`` for the same inputs.  Returns
-    fp32 (dQ, dK, dV).  The workspace (a uint8 CUDA tensor) is allocated here
-    unless given.
+    q, do: [B,H,Nq,d]; k, v: [B,H,Nk,d], all bf16 or all fp16; o fp32
+    [B,H,Nq,d] and lse fp32 [B,H,Nq] as returned by ``forward`` for the same
+    inputs.  Returns fp32 (dQ, dK, dV).  The workspace (a uint8 CUDA tensor)
+    is allocated here unless given.
     """
     import torch
 
-    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
-                        ("do", do, torch.bfloat16), ("o", o, torch.float32), ("lse", lse, torch.float32)):
+    in_dt = q.dtype
+    if in_dt not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v and do must be bf16 or fp16")
+    for name, t, dt in (("q", q, in_dt), ("k", k, in_dt), ("v", v, in_dt),
+                        ("do", do, in_dt), ("o", o, torch.float32), ("lse", lse, torch.float32)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor")
     B, H, Nq, d = q.shape
@@ -274,10 +286,11 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
-        rc = fa2_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
-                          causal, float(scale), workspace.data_ptr(), workspace.numel(),
-                          _stream_handle(stream))
+        rc = fa2_backward_typed(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk,
+                                d, causal, float(scale),
+                                FA2_DTYPE_FP16 if in_dt == torch.float16 else FA2_DTYPE_BF16,
+                                workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
     if rc != FA2_OK:
-        raise FA2Error(rc, "fa2_backward")
+        raise FA2Error(rc, "fa2_backward_typed")
     return dq, dk, dv

@@ -417,10 +417,13 @@ extern "C" size_t fa2_backward_workspace_bytes(int B, int H, int Nq) {
   return bwd_workspace_bytes(static_cast<long long>(B) * H, Nq);
 }
 
-extern "C" int fa2_backward(const void* Q, const void* K, const void* V, const float* O,
-                            const void* dO, const float* LSE, float* dQ, float* dK, float* dV,
-                            int B, int H, int Nq, int Nk, int d, int causal, float scale,
-                            void* workspace, size_t workspace_size, fa2_stream_t stream) {
+namespace {
+
+// The backward pass for bf16 (f16 = false) or fp16 Q, K, V and dO.
+int backward_impl(const void* Q, const void* K, const void* V, const float* O, const void* dO,
+                  const float* LSE, float* dQ, float* dK, float* dV, int B, int H, int Nq, int Nk,
+                  int d, int causal, float scale, void* workspace, size_t workspace_size,
+                  fa2_stream_t stream, bool f16) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA2_ERR_SHAPE;
   const long long BH = static_cast<long long>(B) * H;
   if (BH == 0 || (Nq == 0 && Nk == 0)) return FA2_OK;
@@ -459,17 +462,17 @@ extern "C" int fa2_backward(const void* Q, const void* K, const void* V, const f
     return FA2_ERR_MEMORY;
 
   CUtensorMap mq, mk, mv, mdo, mdq;
-  if (!encode_map(&mq, Q, d, Nq, static_cast<int>(BH), false) ||
-      !encode_map(&mk, K, d, Nk, static_cast<int>(BH), false) ||
-      !encode_map(&mv, V, d, Nk, static_cast<int>(BH), false) ||
-      !encode_map(&mdo, dO, d, Nq, static_cast<int>(BH), false) ||
+  if (!encode_map(&mq, Q, d, Nq, static_cast<int>(BH), f16) ||
+      !encode_map(&mk, K, d, Nk, static_cast<int>(BH), f16) ||
+      !encode_map(&mv, V, d, Nk, static_cast<int>(BH), f16) ||
+      !encode_map(&mdo, dO, d, Nq, static_cast<int>(BH), f16) ||
       !encode_map_f32(&mdq, dQ, d, Nq, static_cast<int>(BH)))
     return FA2_ERR_SHAPE;
 
   const int Nq_pad = (Nq + 127) / 128 * 128;
   float* L2 = static_cast<float*>(workspace);
   float* Dr = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(bh * Nq_pad * 4));
-  if (fa2host::launch_bwd_pre(d, O, dO, LSE, dQ, L2, Dr, static_cast<long long>(bh) * Nq, Nq, Nq_pad,
+  if (fa2host::launch_bwd_pre(d, f16, O, dO, LSE, dQ, L2, Dr, static_cast<long long>(bh) * Nq, Nq, Nq_pad,
                               s) != cudaSuccess)
     return FA2_ERR_LAUNCH;
 
@@ -495,10 +498,30 @@ extern "C" int fa2_backward(const void* Q, const void* K, const void* V, const f
     return FA2_ERR_LAUNCH;
   const long long grid = BH * p.key_blocks;
   if (grid > 0x7fffffffLL) return FA2_ERR_SHAPE;
-  return fa2host::launch_bwd(d, causal != 0, mq, mk, mv, mdo, mdq, p, static_cast<unsigned>(grid), s) ==
+  return fa2host::launch_bwd(d, causal != 0, f16, mq, mk, mv, mdo, mdq, p, static_cast<unsigned>(grid), s) ==
                  cudaSuccess
              ? FA2_OK
              : FA2_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" int fa2_backward(const void* Q, const void* K, const void* V, const float* O,
+                            const void* dO, const float* LSE, float* dQ, float* dK, float* dV,
+                            int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                            void* workspace, size_t workspace_size, fa2_stream_t stream) {
+  return backward_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, workspace,
+                       workspace_size, stream, false);
+}
+
+extern "C" int fa2_backward_typed(const void* Q, const void* K, const void* V, const float* O,
+                                  const void* dO, const float* LSE, float* dQ, float* dK, float* dV,
+                                  int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                  int qkv_dtype, void* workspace, size_t workspace_size,
+                                  fa2_stream_t stream) {
+  if (qkv_dtype != FA2_DTYPE_BF16 && qkv_dtype != FA2_DTYPE_FP16) return FA2_ERR_DTYPE;
+  return backward_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, workspace,
+                       workspace_size, stream, qkv_dtype == FA2_DTYPE_FP16);
 }
 
 extern "C" const char* fa2_status_string(int status) {

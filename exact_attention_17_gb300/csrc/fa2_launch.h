@@ -42,11 +42,12 @@ cudaError_t launch_combine(int d, const float* O_part, const float* LSE_part, in
 // Backward pass (fa2_bwd.cu).
 cudaError_t prepare_bwd();
 // mdq: fp32 [BH][Nq][d] map of dQ, 32-column boxes, 128-byte swizzle (TMA reductions).
-cudaError_t launch_bwd(int d, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
+// f16: Q, K, V and dO are fp16 (else bf16).
+cudaError_t launch_bwd(int d, bool causal, bool f16, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
                        const fa2dev::BwdParams& p, unsigned grid, cudaStream_t s);
 // D_i = dO_i . O_i and LSE_i log2(e) into [BH][Nq_pad] arrays; dQ rows zeroed.
-cudaError_t launch_bwd_pre(int d, const float* O, const void* dO, const float* LSE, float* dQ,
+cudaError_t launch_bwd_pre(int d, bool f16, const float* O, const void* dO, const float* LSE, float* dQ,
                            float* L2, float* Dr, long long rows, int Nq, int Nq_pad, cudaStream_t s);
 cudaError_t launch_zero(float* p, long long n, cudaStream_t s);
 

@@ -218,6 +218,18 @@ int fa2_backward(const void *Q, const void *K, const void *V, const float *O, co
                  int d, int causal, float scale, void *workspace, size_t workspace_size,
                  fa2_stream_t stream);
 
+/*
+ * fa2_backward with fp16 inputs: Q, K, V and dO are all bf16
+ * (qkv_dtype = FA2_DTYPE_BF16, the same as fa2_backward) or all fp16
+ * (FA2_DTYPE_FP16); P and dS are then rounded to that type for their MMAs.
+ * O, LSE, dQ, dK and dV stay fp32.  Other values return FA2_ERR_DTYPE.
+ * Arguments, limits and errors otherwise as fa2_backward.
+ */
+int fa2_backward_typed(const void *Q, const void *K, const void *V, const float *O, const void *dO,
+                       const float *LSE, float *dQ, float *dK, float *dV, int B, int H, int Nq,
+                       int Nk, int d, int causal, float scale, int qkv_dtype, void *workspace,
+                       size_t workspace_size, fa2_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *fa2_status_string(int status);
 

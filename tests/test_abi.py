@@ -173,3 +173,12 @@ def test_fast_division_method():
 def test_wait_check_rejects_out_of_range_limits_on_the_host(lib):
     for t in (0, 999, 10_000_000_001):
         assert fa2.fa2_check_wait_timeout(t) == fa2.FA2_ERR_SHAPE
+
+
+def test_typed_backward_rejects_bad_element_types_on_the_host(lib):
+    args = [16] * 9 + [1, 1, 8, 8, 64, 0, 0.125]
+    for t in (fa2.FA2_DTYPE_FP32, 7, -1):
+        assert fa2.fa2_backward_typed(*args, t, 256, 1 << 20, None) == fa2.FA2_ERR_DTYPE
+    # valid type, empty problem: nothing launched
+    empty = [16] * 9 + [0, 1, 8, 8, 64, 0, 0.125]
+    assert fa2.fa2_backward_typed(*empty, fa2.FA2_DTYPE_FP16, 256, 1 << 20, None) == fa2.FA2_OK

@@ -37,12 +37,12 @@ def gpu_pass(Q, K, V, dO, causal, scale):
     return [t.cpu().double().numpy() for t in (dq, dk, dv)]
 
 
-def check(oracle_mod, Q, K, V, dO, causal, scale, got, heads=None):
+def check(oracle_mod, Q, K, V, dO, causal, scale, got, heads=None, dtype="bf16"):
     """got: (dQ, dK, dV) as [B,H,N,d]; compares the listed flat heads (all by default)."""
     B, H = Q.shape[:2]
     ref = oracle_mod.attention_backward(inputs.bf16_bits(Q), inputs.bf16_bits(K), inputs.bf16_bits(V),
                                         inputs.bf16_bits(dO), causal, scale, heads=heads,
-                                        magnitudes=True)
+                                        dtype=dtype, magnitudes=True)
     hl = list(range(B * H)) if heads is None else list(heads)
     for name, g, r, m in zip(("dQ", "dK", "dV"), got, ref[:3], ref[3:]):
         g = g.reshape(B * H, *g.shape[2:])[hl]
@@ -122,3 +122,24 @@ def test_backward_full_size_sampled_heads(oracle_mod, name, heads):
     check(oracle_mod, Q, K, V, dO, w.causal, w.scale, got, heads=heads)
     for g in got:
         assert np.all(np.isfinite(g))
+
+
+FP16 = [
+    (1, 2, 128, 128, 64, False),
+    (1, 2, 200, 300, 128, True),
+    (2, 1, 513, 129, 128, False),
+    (1, 1, 640, 640, 64, True),
+    (1, 2, 1000, 1000, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", FP16)
+def test_backward_fp16_matches_oracle(oracle_mod, B, H, Nq, Nk, d, causal):
+    """fp16 Q, K, V and dO (fa2_backward_typed): P and dS are rounded to fp16
+    (2^-11 relative per term), inside the same 2^-7 M bound."""
+    seed = 300 + Nq + 3 * Nk + d + int(causal)
+    Q, K, V = inputs.make_qkv(B, H, Nq, Nk, d, seed, qk_std=1.5, dtype=torch.float16)
+    dO = inputs.draw_bf16((B, H, Nq, d), seed, 3, dtype=torch.float16)
+    scale = scale_for(d)
+    got = gpu_pass(Q, K, V, dO, causal, scale)
+    check(oracle_mod, Q, K, V, dO, causal, scale, got, dtype="fp16")
