@@ -236,7 +236,8 @@ def oracle_backward_rate(w, Q, K, V, G, budget_s: float):
     qb, kb, vb, gb = (np.ascontiguousarray(inputs.bf16_bits(t)[:1, :1, :n]) for t in (Q, K, V, G))
     cores = oracle.default_threads()
     t0 = time.perf_counter()
-    oracle.attention_backward(qb, kb, vb, gb, w.causal, w.scale, nthreads=cores)
+    dtype = "fp16" if Q.dtype == torch.float16 else "bf16"
+    oracle.attention_backward(qb, kb, vb, gb, w.causal, w.scale, nthreads=cores, dtype=dtype)
     el = time.perf_counter() - t0
     flops = 2.5 * 4.0 * n * n * w.d / (2 if w.causal else 1)
     return flops / el / 1e12, cores, n, el
@@ -544,10 +545,12 @@ def main():
 def run_backward(args, w, fa2, dev, dist, world, rank):
     """One step = one backward pass (pre-pass + tensor-core kernel) of the
     workload, with O and LSE from one forward pass before the timed region."""
-    if args.dtype != "bf16" or args.num_splits != 1 or args.out_dtype != "fp32":
-        raise SystemExit("--pass backward takes bf16 inputs, fp32 O and no split")
-    Qh, Kh, Vh = inputs.make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.seed, w.qk_dist, w.qk_std, w.v_dist)
-    Gh = inputs.draw_bf16((w.B, w.H, w.Nq, w.d), w.seed, 3)
+    if args.num_splits != 1 or args.out_dtype != "fp32":
+        raise SystemExit("--pass backward takes fp32 O and no split")
+    in_dtype = torch.float16 if args.dtype == "fp16" else torch.bfloat16
+    Qh, Kh, Vh = inputs.make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.seed, w.qk_dist, w.qk_std, w.v_dist,
+                                 dtype=in_dtype)
+    Gh = inputs.draw_bf16((w.B, w.H, w.Nq, w.d), w.seed, 3, dtype=in_dtype)
     Q, K, V, G = (t.to(dev) for t in (Qh, Kh, Vh, Gh))
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -659,14 +662,15 @@ def run_backward(args, w, fa2, dev, dist, world, rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": args.dtype,
         "data": "synthetic",
         "config": dict(workload_config(w, l2_note), **{
-            "pass": "backward", "inputs": "bf16 Q, K, V, dO; fp32 O, LSE",
+            "pass": "backward", "inputs": f"{args.dtype} Q, K, V, dO; fp32 O, LSE",
             "outputs": "fp32 dQ, dK, dV"}),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": roofline_entry(hbm_bound, achieved, peak, peak_src, peaks,
-                                   recorded_traffic(w.name + ":backward", BWD_KERNEL_SOURCES),
+                                   recorded_traffic(w.name + ":backward" + (":fp16" if args.dtype == "fp16" else ""),
+                                                    BWD_KERNEL_SOURCES),
                                    flops, algo, mean_launch_ms, kernel="fa2dev::fa2_bwd_tc_kernel"),
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_tflops(flops, args.e2e_steps, world, e2e_ms), 2),
