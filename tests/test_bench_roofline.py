@@ -36,3 +36,27 @@ def test_algorithmic_bytes_count_each_tensor_once():
     o32, lse = 2 * 8 * 1000 * 64 * 4, 2 * 8 * 1000 * 4
     assert bench.algorithmic_bytes(w) == q + 2 * kv + o32 + lse
     assert bench.algorithmic_bytes(w, 2) == q + 2 * kv + o32 // 2 + lse
+
+
+def test_traffic_records_follow_the_kernel_source():
+    """A recorded DRAM figure is reported only for the translation unit it was
+    taken on and only while the kernel sources hash to the recorded value."""
+    import json
+    import os
+
+    sources = bench.fwd_kernel_sources(128)
+    assert sources[-1].endswith("fa2_tc_d128_bf16.cu")
+    assert bench.fwd_kernel_sources(256, fp16=True)[-1].endswith("fa2_tc_d256_f16.cu")
+    with open(os.path.join(bench.ROOT, "profiles", "dram_traffic.json")) as f:
+        rec = json.load(f)
+    for name, entry in rec.items():
+        if name.endswith(":backward"):
+            srcs = bench.BWD_KERNEL_SOURCES
+        else:
+            srcs = bench.fwd_kernel_sources(inputs.workload(name).d)
+        if entry["kernel_source_hash"] == bench.kernel_source_hash(srcs):
+            assert bench.recorded_traffic(name, srcs) == entry["dram_bytes_per_launch"]
+        # another translation unit (fp16) never picks up a bf16 record
+        if not name.endswith(":backward"):
+            assert bench.recorded_traffic(name, bench.fwd_kernel_sources(inputs.workload(name).d, True)) is None
+    assert bench.recorded_traffic("no_such_workload", sources) is None
