@@ -342,10 +342,10 @@ extern "C" int fa2_forward_splitkv(const void* Q, const void* K, const void* V, 
                                    int B, int H, int Nq, int Nk, int d, int causal, float scale,
                                    int num_splits, void* workspace, size_t workspace_size,
                                    fa2_stream_t stream) {
+  if (num_splits < 1 || num_splits > kMaxSplits) return FA2_ERR_SHAPE;
   Problem pr;
   int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr);
   if (rc != FA2_OK || pr.empty) return rc;
-  if (num_splits < 1 || num_splits > kMaxSplits) return FA2_ERR_SHAPE;
   int splits = 1, tps = 1;
   split_plan(Nk, num_splits, &splits, &tps);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -587,8 +587,8 @@ extern "C" int fa2_device_status(fa2_stream_t stream, int reset) {
 //
 // The scratch is one file-scope device array.  Host code must not pass the
 // array's name to a kernel: on the host it is only a stand-in for the symbol.
-// Its device address is looked up once per device, with that device current,
-// by the first call on the device.  All calls share the array and it keeps
+// Its device address is looked up per device, with that device current, by
+// the first call on the device (again by the next call if that lookup failed).  All calls share the array and it keeps
 // the last call's contents; nothing in it needs to start at zero, because the
 // partial-results kernel writes every entry the merge kernel reads.  Calls
 // whose kernels overlap on the GPU (different streams, or different host
@@ -599,12 +599,29 @@ constexpr size_t kStaticScratchBytes = static_cast<size_t>(32) << 20;  // 32 MiB
 
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kStaticScratchBytes];
 
+// Device address of the array on the current device (nullptr on failure).
+// Only a successful lookup is kept: a lookup that failed (for example one
+// made during a stream capture) is retried by the next call, and its error
+// is cleared so that it cannot surface in a later, unrelated check.
 struct StaticScratch {
-  std::once_flag once;
+  std::mutex mu;
   void* ptr = nullptr;
-  cudaError_t err = cudaErrorNotReady;
 };
 StaticScratch g_static_scratch[kMaxDevices];
+
+void* static_scratch_address(int dev) {
+  StaticScratch& st = g_static_scratch[dev];
+  std::lock_guard<std::mutex> lock(st.mu);
+  if (st.ptr == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_splitkv_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    st.ptr = p;
+  }
+  return st.ptr;
+}
 
 }  // namespace
 
@@ -612,10 +629,10 @@ extern "C" int fa2_forward_splitkv_static(const void* Q, const void* K, const vo
                                           float* LSE, int B, int H, int Nq, int Nk, int d,
                                           int causal, float scale, int num_splits,
                                           fa2_stream_t stream) {
+  if (num_splits < 1 || num_splits > kMaxSplits) return FA2_ERR_SHAPE;
   Problem pr;
   int rc = validate(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, &pr);
   if (rc != FA2_OK || pr.empty) return rc;
-  if (num_splits < 1 || num_splits > kMaxSplits) return FA2_ERR_SHAPE;
   int splits = 1, tps = 1;
   split_plan(Nk, num_splits, &splits, &tps);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -626,15 +643,12 @@ extern "C" int fa2_forward_splitkv_static(const void* Q, const void* K, const vo
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA2_ERR_DEVICE;
-  StaticScratch& st = g_static_scratch[dev];
-  std::call_once(st.once, [&] {
-    st.err = cudaGetSymbolAddress(&st.ptr, g_splitkv_scratch);
-  });
-  if (st.err != cudaSuccess || st.ptr == nullptr) return FA2_ERR_LAUNCH;
+  void* scratch = static_scratch_address(dev);
+  if (scratch == nullptr) return FA2_ERR_LAUNCH;
 
   const size_t rows = static_cast<size_t>(pr.BH) * Nq;
-  float* O_part = static_cast<float*>(st.ptr);
-  float* LSE_part = reinterpret_cast<float*>(static_cast<char*>(st.ptr) +
+  float* O_part = static_cast<float*>(scratch);
+  float* LSE_part = reinterpret_cast<float*>(static_cast<char*>(scratch) +
                                              align256(static_cast<size_t>(splits) * rows * d * 4));
   rc = launch_forward(Q, K, V, O, LSE, pr, causal, scale, splits, tps, O_part, LSE_part, s);
   if (rc != FA2_OK) return rc;

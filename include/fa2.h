@@ -168,7 +168,8 @@ int fa2_merge(const float *O_parts, const float *LSE_parts, int num_parts, long 
  * actually used exceeds 32 MiB, is rejected with FA2_ERR_SCRATCH and nothing
  * is launched.  The first call on a device looks up the array's device
  * address (with that device current); make that first call before any
- * stream capture.  All calls share the array: calls whose kernels may
+ * stream capture.  If the lookup fails the call returns FA2_ERR_LAUNCH and
+ * the next call tries again.  All calls share the array: calls whose kernels may
  * overlap on the GPU (other streams, other host threads) race on it and
  * must be serialised by the caller.  The array keeps the last call's
  * contents; no call depends on them.  The function never calls cudaMalloc,

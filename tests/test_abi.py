@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(10):
+    for code in range(12):
         s = fa2.fa2_status_string(code)
         assert s and s != "unknown status"
     assert fa2.fa2_status_string(12345) == "unknown status"
@@ -52,9 +52,25 @@ def call(**kw):
                            args["scale"], args["stream"])
 
 
-@pytest.mark.parametrize("fn", ["fa2_forward", "fa2_forward_simt"])
+def _split_static(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, stream, num_splits=4):
+    return fa2.fa2_forward_splitkv_static(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale,
+                                          num_splits, stream)
+
+
+def _split_workspace(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, stream, num_splits=4):
+    return fa2.fa2_forward_splitkv(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, num_splits,
+                                   256, 1 << 20, stream)
+
+
+FORWARD_ENTRY_POINTS = {"fa2_forward": lambda: fa2.fa2_forward,
+                        "fa2_forward_simt": lambda: fa2.fa2_forward_simt,
+                        "fa2_forward_splitkv": lambda: _split_workspace,
+                        "fa2_forward_splitkv_static": lambda: _split_static}
+
+
+@pytest.mark.parametrize("fn", sorted(FORWARD_ENTRY_POINTS))
 def test_host_side_argument_errors(lib, fn):
-    f = getattr(fa2, fn)
+    f = FORWARD_ENTRY_POINTS[fn]()
 
     def c(**kw):
         a = dict(Q=16, K=16, V=16, O=16, LSE=16, B=1, H=1, Nq=8, Nk=8, d=64, causal=0,
@@ -83,6 +99,17 @@ def test_host_side_argument_errors(lib, fn):
     for name in ("Q", "K", "V", "O"):
         assert c(**{name: 24}) == fa2.FA2_ERR_ALIGN
     assert c(LSE=18) == fa2.FA2_ERR_ALIGN
+
+
+@pytest.mark.parametrize("fn", [_split_static, _split_workspace])
+def test_split_entry_points_check_the_split_count_first(lib, fn):
+    args = (16, 16, 16, 16, 16, 1, 1, 8, 8, 64, 0, 0.125, None)
+    for n in (0, -1, 65, 1000):
+        assert fn(*args, num_splits=n) == fa2.FA2_ERR_SHAPE
+    # a valid count on an empty problem launches nothing
+    empty = (16, 16, 16, 16, 16, 0, 1, 8, 8, 64, 0, 0.125, None)
+    assert fn(*empty, num_splits=64) == fa2.FA2_OK
+    assert fn(*empty, num_splits=1) == fa2.FA2_OK
 
 
 def test_typed_entry_point_rejects_bad_element_types_on_the_host(lib):
