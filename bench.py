@@ -268,7 +268,7 @@ def run_reference(args, w):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1000 * secs / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w, "oracle on host cores"),
+        "data": "synthetic", "config": forward_config(w, args),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -297,7 +297,7 @@ def run_reference_backward(args, w, Q, K, V):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1000 * secs / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": dict(workload_config(w, "oracle on host cores"), **{"pass": "backward"}),
+        "data": "synthetic", "config": backward_config(w, args),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -306,6 +306,39 @@ def run_reference_backward(args, w, Q, K, V):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def forward_l2_note(w):
+    """Whether the forward arm flushes L2 between steps (inputs that would fit
+    twice in L2 are flushed), as the note the config carries."""
+    in_bytes = 2 * w.B * w.H * (w.Nq + 2 * w.Nk) * w.d
+    if in_bytes <= 2 * L2_BYTES:
+        return True, "L2 flushed between steps (256 MiB write, outside the kernel events)"
+    return False, f"inputs {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"
+
+
+def backward_l2_note(w):
+    in_bytes = algorithmic_bytes_backward(w)
+    if in_bytes <= 2 * L2_BYTES:
+        return True, "L2 flushed between steps (256 MiB write, outside the kernel events)"
+    return False, f"operands {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"
+
+
+def forward_config(w, args):
+    """The config object of the forward arms (the same for the GPU arm and the
+    reference arm, so that the two lines describe one workload)."""
+    return dict(workload_config(w, forward_l2_note(w)[1]), num_splits=args.num_splits,
+                inputs=f"{args.dtype} BHSD",
+                outputs=f"{'fp32' if args.out_dtype == 'fp32' else args.dtype} O, fp32 LSE")
+
+
+def backward_config(w, args):
+    return dict(workload_config(w, backward_l2_note(w)[1]), **{
+        "pass": "backward", "inputs": f"{args.dtype} Q, K, V, dO; fp32 O, LSE",
+        "outputs": "fp32 dQ, dK, dV"})
 
 
 def workload_config(w, l2_note):
@@ -342,6 +375,19 @@ def roofline_entry(hbm_bound, achieved_tflops, peak_tflops, peak_src, peaks, tra
                 **common)
 
 
+def relaunch_distributed(n: int) -> int:
+    """Run this same command as n ranks (one process per GPU) under
+    torch.distributed.run on 127.0.0.1 and return its exit status."""
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.run(cmd).returncode
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -361,6 +407,10 @@ def main():
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count (smaller profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunks", type=int, default=4,
+                    help="groups of heads the end-to-end call pipelines its copies over")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads measured beside the headline one")
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
                     help="time the forward pass (default) or the backward pass")
     args = ap.parse_args()
@@ -370,6 +420,16 @@ def main():
         w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_heads{args.heads}")
     if args.reference_step_s is None:
         args.reference_step_s = max(1.0, min(10.0, 120.0 / max(1, args.steps)))
+
+    world_env = os.environ.get("WORLD_SIZE")
+    if world_env is None and args.gpus > 1:
+        return relaunch_distributed(args.gpus)
+    if world_env is not None and int(world_env) != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world_env}", file=sys.stderr)
+        return 2
+    if args.gpus < 1:
+        print("bench.py: --gpus must be >= 1", file=sys.stderr)
+        return 2
 
     if args.impl == "reference":
         return run_reference(args, w)
@@ -401,14 +461,9 @@ def main():
     O = torch.empty(w.B, w.H, w.Nq, w.d, device=dev, dtype=out_dtype)
     L = torch.empty(w.B, w.H, w.Nq, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    in_bytes = (Q.numel() + K.numel() + V.numel()) * 2
-    l2_bytes = 129 * 1024 * 1024
     flush = None
-    if in_bytes <= 2 * l2_bytes:
+    if forward_l2_note(w)[0]:
         flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
-        l2_note = "L2 flushed between steps (256 MiB write, outside the kernel events)"
-    else:
-        l2_note = f"inputs {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"
 
     workspace = None
     if args.num_splits > 1:
@@ -456,12 +511,23 @@ def main():
     timed_ms = kernel_ms if flush is not None else total_ms
     job_ms = job_time_ms(timed_ms, dist, dev)
 
-    # end to end through the public call: pinned host inputs -> device -> forward -> host result
+    # End to end through the public call with host buffers: pinned host
+    # inputs -> device -> forward -> host result.  With bf16 inputs, fp32 O
+    # and no split this is fa2_forward_host, which overlaps the copies of one
+    # group of heads with the computation of another; otherwise the copies
+    # and the forward run one after another on the stream.
     Qp, Kp, Vp = Qh.pin_memory(), Kh.pin_memory(), Vh.pin_memory()
     Op = torch.empty(O.shape, dtype=out_dtype).pin_memory()
     Lp = torch.empty(L.shape, dtype=torch.float32).pin_memory()
+    pipelined = args.dtype == "bf16" and args.out_dtype == "fp32" and args.num_splits == 1
+    e2e_kind = (f"fa2_forward_host, {args.e2e_chunks} head groups pipelined over copy/compute streams"
+                if pipelined else "copies and forward in order on one stream")
 
     def e2e_step():
+        if pipelined:
+            fa2.forward_host(Qp, Kp, Vp, causal=w.causal, scale=w.scale, out=Op, lse=Lp,
+                             device_buffers=(Q, K, V, O, L), chunks=args.e2e_chunks, stream=stream)
+            return
         Q.copy_(Qp, non_blocking=True)
         K.copy_(Kp, non_blocking=True)
         V.copy_(Vp, non_blocking=True)
@@ -524,22 +590,134 @@ def main():
         "vs_baseline": None,
         "dtype": args.dtype,
         "data": "synthetic",
-        "config": dict(workload_config(w, l2_note), num_splits=args.num_splits,
-                       inputs=f"{args.dtype} BHSD", outputs=f"{'fp32' if args.out_dtype == 'fp32' else args.dtype} O, fp32 LSE"),
+        "config": forward_config(w, args),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": roofline_entry(hbm_bound, achieved, peak, peak_src, peaks, traffic, w.flops,
                                    algo_bytes, mean_launch_ms),
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_tflops(w.flops, args.e2e_steps, world, e2e_ms), 2),
-                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms / args.e2e_steps, 4), "how": e2e_kind},
         "gpu_launches": args.steps * (2 if args.num_splits > 1 else 1),
         "clocks": clk,
     }
+    if not args.no_workloads and args.heads is None:
+        line["workloads"] = other_workloads(fa2, dev, w.name, peaks, peak_src)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
 
+
+
+# Measured beside the headline workload, each with its own roof.  The
+# 4096-length causal case and the cross-length case are two of the five
+# workloads; the non-causal 16384-length case is the same shape as the
+# headline without the mask; the 1000-length case runs split-KV with the
+# library's recommended split count; the one-tile case reports the host cost
+# of a call next to its device time.
+OTHER_WORKLOADS = ["b4_h16_n4096_d128_causal", "b16_h32_nq128_nk8192_d128", "b1_h32_n16384_d128",
+                   "b2_h8_n1000_d64", "b1_h1_n128_d64"]
+
+
+def measure_launches(fa2, dev, w, steps=10, warmup=3, num_splits=1):
+    """Mean CUDA-event time of one forward call of workload w on its own
+    stream (inputs resident; L2 flushed between launches when the inputs
+    would fit in it)."""
+    Qh, Kh, Vh = inputs.workload_inputs(w)
+    Q, K, V = Qh.to(dev), Kh.to(dev), Vh.to(dev)
+    del Qh, Kh, Vh
+    O = torch.empty(w.B, w.H, w.Nq, w.d, device=dev)
+    L = torch.empty(w.B, w.H, w.Nq, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    in_bytes = (Q.numel() + K.numel() + V.numel()) * 2
+    flush = None
+    if in_bytes <= 2 * 129 * 1024 * 1024:
+        flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    workspace = None
+    if num_splits > 1:
+        need = fa2.fa2_splitkv_workspace_bytes(w.B, w.H, w.Nq, w.d, num_splits)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+
+    def call():
+        fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, out=O, lse=L, stream=stream,
+                    num_splits=num_splits, workspace=workspace)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(steps):
+            if flush is not None:
+                flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+    if fa2.fa2_device_status(None, reset=True) != fa2.FA2_OK:
+        raise SystemExit(f"device status error while timing {w.name}")
+    note = ("L2 flushed between launches (256 MiB write, outside the events)" if flush is not None
+            else f"inputs {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush")
+    extra = {}
+    if w.B * w.H * w.Nq <= 128:
+        # host cost of one call: back-to-back calls without synchronisation
+        n = 200
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            t0 = time.perf_counter()
+            for _ in range(n):
+                call()
+            t1 = time.perf_counter()
+            b.record(stream)
+            b.synchronize()
+        args = (Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), L.data_ptr(), w.B, w.H, w.Nq,
+                w.Nk, w.d, int(w.causal), w.scale, stream.cuda_stream)
+        t2 = time.perf_counter()
+        for _ in range(n):
+            fa2.fa2_forward(*args)
+        t3 = time.perf_counter()
+        torch.cuda.synchronize(dev)
+        extra = {"host_us_per_call_python": round(1e6 * (t1 - t0) / n, 2),
+                 "host_us_per_call_c_abi": round(1e6 * (t3 - t2) / n, 2),
+                 "device_us_per_call_back_to_back": round(1000 * a.elapsed_time(b) / n, 2)}
+    del Q, K, V, O, L, flush, workspace
+    torch.cuda.empty_cache()
+    return statistics.mean(ms), note, extra
+
+
+def other_workloads(fa2, dev, headline, peaks, peak_src):
+    out = {}
+    peak = float(peaks["bf16_tflops"])
+    balance = peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    for name in OTHER_WORKLOADS:
+        if name == headline:
+            continue
+        w = inputs.workload(name)
+        splits = 1
+        if name == "b2_h8_n1000_d64":
+            splits = fa2.fa2_splitkv_recommended_splits(w.B, w.H, w.Nq, w.Nk, 0)
+        ms, note, extra = measure_launches(fa2, dev, w, num_splits=splits)
+        tf = w.flops / (ms * 1e-3) / 1e12
+        algo = algorithmic_bytes(w)
+        hbm_bound = w.flops / algo < balance
+        entry = {"config": {"B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+                            "num_splits": splits, "l2": note},
+                 "mean_launch_ms": round(ms, 4), "tflops": round(tf, 2),
+                 "pct_of_peak": round(100 * tf / peak, 2),
+                 "kernels_per_call": 2 if splits > 1 else 1,
+                 "roofline": roofline_entry(hbm_bound, tf, peak, peak_src, peaks,
+                                            recorded_traffic(name, fwd_kernel_sources(w.d)), w.flops,
+                                            algo, ms)}
+        entry.update(extra)
+        out[name] = entry
+    return out
 
 
 def run_backward(args, w, fa2, dev, dist, world, rank):
@@ -560,14 +738,9 @@ def run_backward(args, w, fa2, dev, dist, world, rank):
         dV = torch.empty(w.B, w.H, w.Nk, w.d, device=dev)
         ws = torch.empty(max(fa2.fa2_backward_workspace_bytes(w.B, w.H, w.Nq), 1), dtype=torch.uint8,
                          device=dev)
-    in_bytes = algorithmic_bytes_backward(w)
-    l2_bytes = 129 * 1024 * 1024
     flush = None
-    if in_bytes <= 2 * l2_bytes:
+    if backward_l2_note(w)[0]:
         flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
-        l2_note = "L2 flushed between steps (256 MiB write, outside the kernel events)"
-    else:
-        l2_note = f"operands {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"
 
     def step(s):
         fa2.backward(Q, K, V, O, L, G, causal=w.causal, scale=w.scale, dq=dQ, dk=dK, dv=dV,
@@ -664,9 +837,7 @@ def run_backward(args, w, fa2, dev, dist, world, rank):
         "vs_baseline": None,
         "dtype": args.dtype,
         "data": "synthetic",
-        "config": dict(workload_config(w, l2_note), **{
-            "pass": "backward", "inputs": f"{args.dtype} Q, K, V, dO; fp32 O, LSE",
-            "outputs": "fp32 dQ, dK, dV"}),
+        "config": backward_config(w, args),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": roofline_entry(hbm_bound, achieved, peak, peak_src, peaks,
                                    recorded_traffic(w.name + ":backward" + (":fp16" if args.dtype == "fp16" else ""),

@@ -40,6 +40,8 @@ SIGNATURES = {
     "fa2_forward_typed": (_I, _FORWARD_ARGS[:-1] + [_I, _I, _P]),
     "fa2_splitkv_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "fa2_forward_splitkv": (_I, _FORWARD_ARGS[:-1] + [_I, _P, _Z, _P]),
+    "fa2_splitkv_recommended_splits": (_I, [_I, _I, _I, _I, _I]),
+    "fa2_forward_host": (_I, [_P] * 10 + [_I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa2_merge": (_I, [_P, _P, _I, _LL, _I, _P, _P, _P]),
     "fa2_forward_splitkv_static": (_I, _FORWARD_ARGS[:-1] + [_I, _P]),
     "fa2_backward_workspace_bytes": (_Z, [_I, _I, _I]),
@@ -111,6 +113,18 @@ def fa2_forward_splitkv_static(Q, K, V, O, LSE, B, H, Nq, Nk, d, causal, scale, 
                                                 int(bool(causal)), scale, num_splits, stream)
 
 
+def fa2_splitkv_recommended_splits(B, H, Nq, Nk, sm_count=0) -> int:
+    """Split count that fills the GPU for fa2_forward_splitkv (see fa2.h)."""
+    return library().fa2_splitkv_recommended_splits(B, H, Nq, Nk, sm_count)
+
+
+def fa2_forward_host(Qh, Kh, Vh, Oh, LSEh, Qd, Kd, Vd, Od, LSEd, B, H, Nq, Nk, d, causal, scale,
+                     chunks, stream) -> int:
+    """Raw C call of the forward pass from host memory, pipelined over groups of heads."""
+    return library().fa2_forward_host(Qh, Kh, Vh, Oh, LSEh, Qd, Kd, Vd, Od, LSEd, B, H, Nq, Nk, d,
+                                      int(bool(causal)), scale, chunks, stream)
+
+
 def fa2_merge(O_parts, LSE_parts, num_parts, rows, d, O, LSE, stream) -> int:
     """Raw C call of the merge of partial attention results."""
     return library().fa2_merge(O_parts, LSE_parts, num_parts, rows, d, O, LSE, stream)
@@ -167,6 +181,8 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     cross-check implementation instead of the tensor-core one.
     ``num_splits > 1`` runs the split-KV forward over that many key ranges;
     its workspace (a uint8 CUDA tensor) is allocated here unless given.
+    ``num_splits="auto"`` takes the count fa2_splitkv_recommended_splits gives
+    for the problem on q's device (1 when the grid already fills the GPU).
     """
     import torch
 
@@ -193,6 +209,9 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     for name, t, shape, dt in (("out", out, (B, H, Nq, d), out_dtype), ("lse", lse, (B, H, Nq), torch.float32)):
         if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
             raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shape} on {q.device}")
+    if num_splits == "auto":
+        with torch.cuda.device(q.device):
+            num_splits = fa2_splitkv_recommended_splits(B, H, Nq, Nk, 0)
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
             B, H, Nq, Nk, d, causal, float(scale))
     codes = {torch.bfloat16: FA2_DTYPE_BF16, torch.float16: FA2_DTYPE_FP16, torch.float32: FA2_DTYPE_FP32}
@@ -217,6 +236,55 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
             name = "fa2_forward" if impl == "tc" else "fa2_forward_simt"
     if rc != FA2_OK:
         raise FA2Error(rc, name)
+    return out, lse
+
+
+def forward_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                 device_buffers=None, chunks: int = 4, stream=None):
+    """Attention forward with inputs and outputs in host memory (fa2_forward_host).
+
+    q: [B,H,Nq,d], k, v: [B,H,Nk,d] contiguous bf16 CPU tensors (pinned
+    memory lets the copies overlap the computation).  Returns (O, LSE) as
+    fp32 CPU tensors (``out``/``lse`` if given; pinned when allocated here).
+    ``device_buffers`` = (q_dev, k_dev, v_dev, o_dev, lse_dev) CUDA tensors of
+    the full sizes, allocated on the current device unless given.  The call
+    is asynchronous on ``stream``: synchronise it before reading the result.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CPU tensor")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d] matching q")
+    if scale is None:
+        scale = float(torch.tensor(d, dtype=torch.float64).rsqrt().float())
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.float32).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+    for name, t, shape in (("out", out, (B, H, Nq, d)), ("lse", lse, (B, H, Nq))):
+        if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous() or t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous fp32 CPU tensor of shape {shape}")
+    if device_buffers is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        device_buffers = (torch.empty_like(q, device=dev), torch.empty_like(k, device=dev),
+                          torch.empty_like(v, device=dev), torch.empty(out.shape, device=dev),
+                          torch.empty(lse.shape, device=dev))
+    qd, kd, vd, od, ld = device_buffers
+    for name, t, ref in (("q_dev", qd, q), ("k_dev", kd, k), ("v_dev", vd, v), ("o_dev", od, out),
+                         ("lse_dev", ld, lse)):
+        if (not t.is_cuda or t.dtype != ref.dtype or tuple(t.shape) != tuple(ref.shape)
+                or not t.is_contiguous() or t.device != qd.device):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor like {name[:-4]} on one device")
+    with torch.cuda.device(qd.device):
+        rc = fa2_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                              qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), ld.data_ptr(),
+                              B, H, Nq, Nk, d, causal, float(scale), int(chunks), _stream_handle(stream))
+    if rc != FA2_OK:
+        raise FA2Error(rc, "fa2_forward_host")
     return out, lse
 
 

@@ -85,19 +85,76 @@ int sm_count() {
   return g_devices[dev].sms > 0 ? g_devices[dev].sms : 148;
 }
 
+// Allocations (base address, size) already found to be device or managed
+// memory.  The range query below runs on every call and returns the live
+// allocation holding a pointer; only the memory-type query is skipped for an
+// allocation seen before.  An allocation freed and replaced by another at
+// the same base with the same size is looked up again only if the range
+// query fails for it (memory that is not a device allocation).
+struct AllocCache {
+  static constexpr int kEntries = 32;
+  std::mutex mu;
+  CUdeviceptr base[kEntries] = {};
+  size_t size[kEntries] = {};
+  int next = 0;
+
+  bool hit(CUdeviceptr b, size_t n) {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < kEntries; ++i)
+      if (base[i] == b && size[i] == n && n != 0) return true;
+    return false;
+  }
+  void add(CUdeviceptr b, size_t n) {
+    std::lock_guard<std::mutex> lock(mu);
+    base[next] = b;
+    size[next] = n;
+    next = (next + 1) % kEntries;
+  }
+};
+AllocCache g_alloc_cache;
+
 // The whole byte range [p, p + bytes) must be device memory of one allocation.
+// The cheap range query comes first; when it fails (it also fails before the
+// runtime has made the device's context current on this thread), the memory
+// type query, which makes it current, runs and the range query is repeated.
 bool device_range_ok(const void* p, size_t bytes) {
+  const uintptr_t begin = reinterpret_cast<uintptr_t>(p);
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  bool have_range = driver().range(&base, &size, static_cast<CUdeviceptr>(begin)) == CUDA_SUCCESS;
+  if (have_range && !(begin >= base && bytes <= size && begin - base <= size - bytes)) return false;
+  if (have_range && g_alloc_cache.hit(base, size)) return true;
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
   if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return false;
-  CUdeviceptr base = 0;
-  size_t size = 0;
-  if (driver().range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return false;
-  const uintptr_t begin = reinterpret_cast<uintptr_t>(p);
-  return begin >= base && bytes <= size && begin - base <= size - bytes;
+  if (!have_range) {
+    if (driver().range(&base, &size, static_cast<CUdeviceptr>(begin)) != CUDA_SUCCESS) return false;
+    if (!(begin >= base && bytes <= size && begin - base <= size - bytes)) return false;
+  }
+  g_alloc_cache.add(base, size);
+  return true;
+}
+
+// Device address of the status word on the current device (looked up once
+// per device; a failed lookup is retried by the next call).
+int* status_word() {
+  static std::mutex mu;
+  static int* addr[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
 }
 
 // 3-D map over [BH][N][d] 16-bit elements (bf16 or fp16): box = 64 columns
@@ -264,8 +321,8 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   p.div_group = make_fast_div(p.item_group);
   p.div_splits = make_fast_div(splits);
   p.wave = sm_count() * (subs == 2 || d == 256 ? 1 : 2);
-  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
-    return FA2_ERR_LAUNCH;
+  p.status = status_word();
+  if (p.status == nullptr) return FA2_ERR_LAUNCH;
 
   const unsigned grid = static_cast<unsigned>(blocks * pr.BH * splits);
   const bool c = causal != 0;
@@ -336,6 +393,54 @@ extern "C" int fa2_forward_typed(const void* Q, const void* K, const void* V, vo
 extern "C" size_t fa2_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
   if (B < 0 || H < 0 || Nq < 0 || num_splits < 1 || !forward_head_dim(d)) return 0;
   return workspace_bytes(static_cast<long long>(B) * H, Nq, d, num_splits);
+}
+
+namespace {
+
+// Split count for fa2_forward_splitkv on a machine with `sms` SMs.  Without a
+// split every (b*H + h, query block) is one CTA of one 128-row sub-tile, two
+// of which run on each SM; with S key ranges there are S times as many CTAs,
+// each visiting about 1/S of the key tiles.  The estimate of the time is
+// (waves of CTAs) x (key tiles per CTA + 1), the 1 standing for a CTA's
+// fixed start and end costs; the smallest S with the least estimate wins.
+// Only grids that leave CTA slots empty are split: a grid of a wave or more
+// keeps S = 1.
+int recommended_splits(long long BH, int Nq, int Nk, int sms) {
+  if (BH <= 0 || Nq <= 0 || Nk <= 0 || sms <= 0) return 1;
+  const long long ctas = (static_cast<long long>(Nq) + 127) / 128 * BH;
+  const long long slots = 2LL * sms;
+  if (ctas >= slots) return 1;
+  const int tiles = key_tiles(Nk);
+  int best = 1;
+  long long best_cost = -1;
+  for (int want = 1; want <= kMaxSplits && want <= tiles; ++want) {
+    int splits = 1, tps = 1;
+    split_plan(Nk, want, &splits, &tps);
+    if (splits != want) continue;   // the same plan as a smaller count
+    const long long waves = (ctas * splits + slots - 1) / slots;
+    const long long cost = waves * (tps + 1);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = splits;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+extern "C" int fa2_splitkv_recommended_splits(int B, int H, int Nq, int Nk, int sm_count) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return 1;
+  int sms = sm_count;
+  if (sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 1;
+    }
+  }
+  return recommended_splits(static_cast<long long>(B) * H, Nq, Nk, sms);
 }
 
 extern "C" int fa2_forward_splitkv(const void* Q, const void* K, const void* V, float* O, float* LSE,
@@ -494,8 +599,8 @@ int backward_impl(const void* Q, const void* K, const void* V, const float* O, c
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = kWaitTimeoutNs;
-  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p.status), g_device_status) != cudaSuccess)
-    return FA2_ERR_LAUNCH;
+  p.status = status_word();
+  if (p.status == nullptr) return FA2_ERR_LAUNCH;
   const long long grid = BH * p.key_blocks;
   if (grid > 0x7fffffffLL) return FA2_ERR_SHAPE;
   return fa2host::launch_bwd(d, causal != 0, f16, mq, mk, mv, mdo, mdq, p, static_cast<unsigned>(grid), s) ==
@@ -563,9 +668,8 @@ extern "C" int fa2_check_wait_timeout(unsigned long long timeout_ns, fa2_stream_
   if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return FA2_ERR_SHAPE;
   const int rc = device_ready();
   if (rc != FA2_OK) return rc;
-  int* status = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_device_status) != cudaSuccess)
-    return FA2_ERR_LAUNCH;
+  int* status = status_word();
+  if (status == nullptr) return FA2_ERR_LAUNCH;
   fa2dev::fa2_wait_check_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, timeout_ns);
   return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
 }
@@ -656,4 +760,109 @@ extern "C" int fa2_forward_splitkv_static(const void* Q, const void* K, const vo
                  cudaSuccess
              ? FA2_OK
              : FA2_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Forward pass from host memory, pipelined over groups of heads: while one
+// group computes, the next one's inputs are copied in and the previous one's
+// outputs are copied out.  Three streams per device (copies in, compute,
+// copies out) and their events are created by the first call on the device
+// and kept; a mutex serialises the enqueueing so that two host threads do
+// not interleave their event records.
+namespace {
+
+constexpr int kMaxChunks = 16;
+
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t in = nullptr, compute = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t loaded[kMaxChunks] = {};
+  cudaEvent_t computed[kMaxChunks] = {};
+};
+HostPipe g_pipes[kMaxDevices];
+
+bool make_pipe(HostPipe& hp) {
+  const unsigned ef = cudaEventDisableTiming;
+  bool ok = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.compute, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.start, ef) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.done, ef) == cudaSuccess;
+  for (int c = 0; ok && c < kMaxChunks; ++c)
+    ok = cudaEventCreateWithFlags(&hp.loaded[c], ef) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp.computed[c], ef) == cudaSuccess;
+  if (!ok) cudaGetLastError();
+  return ok;
+}
+
+}  // namespace
+
+extern "C" int fa2_forward_host(const void* Qh, const void* Kh, const void* Vh, float* Oh, float* LSEh,
+                                void* Qd, void* Kd, void* Vd, float* Od, float* LSEd, int B, int H,
+                                int Nq, int Nk, int d, int causal, float scale, int chunks,
+                                fa2_stream_t stream) {
+  if (chunks < 1 || chunks > kMaxChunks) return FA2_ERR_SHAPE;
+  Problem pr;
+  int rc = validate(Qd, Kd, Vd, Od, LSEd, B, H, Nq, Nk, d, scale, &pr);
+  if (rc != FA2_OK || pr.empty) return rc;
+  if (!Qh || !Kh || !Vh || !Oh || !LSEh) return FA2_ERR_NULL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA2_ERR_DEVICE;
+  HostPipe& hp = g_pipes[dev];
+  std::lock_guard<std::mutex> lock(hp.mu);
+  if (!hp.ready) {
+    if (!make_pipe(hp)) return FA2_ERR_LAUNCH;
+    hp.ready = true;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long long BH = pr.BH;
+  const int n = static_cast<int>(chunks < BH ? chunks : BH);
+  // the pipeline starts after the work already queued on the caller's stream
+  bool ok = cudaEventRecord(hp.start, s) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.in, hp.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.compute, hp.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp.out, hp.start, 0) == cudaSuccess;
+  const size_t q_head = static_cast<size_t>(Nq) * d, kv_head = static_cast<size_t>(Nk) * d;
+  for (int c = 0; c < n && ok; ++c) {
+    const long long h0 = BH * c / n, h1 = BH * (c + 1) / n;
+    const size_t nh = static_cast<size_t>(h1 - h0), off = static_cast<size_t>(h0);
+    const char* qh = static_cast<const char*>(Qh) + off * q_head * 2;
+    const char* kh = static_cast<const char*>(Kh) + off * kv_head * 2;
+    const char* vh = static_cast<const char*>(Vh) + off * kv_head * 2;
+    char* qd = static_cast<char*>(Qd) + off * q_head * 2;
+    char* kd = static_cast<char*>(Kd) + off * kv_head * 2;
+    char* vd = static_cast<char*>(Vd) + off * kv_head * 2;
+    ok = cudaMemcpyAsync(qd, qh, nh * q_head * 2, cudaMemcpyDefault, hp.in) == cudaSuccess &&
+         cudaMemcpyAsync(kd, kh, nh * kv_head * 2, cudaMemcpyDefault, hp.in) == cudaSuccess &&
+         cudaMemcpyAsync(vd, vh, nh * kv_head * 2, cudaMemcpyDefault, hp.in) == cudaSuccess &&
+         cudaEventRecord(hp.loaded[c], hp.in) == cudaSuccess &&
+         cudaStreamWaitEvent(hp.compute, hp.loaded[c], 0) == cudaSuccess;
+    if (!ok) break;
+    Problem sub = pr;
+    sub.B = 1;
+    sub.H = static_cast<int>(nh);
+    sub.BH = static_cast<long long>(nh);
+    float* od = Od + off * q_head;
+    float* ld = LSEd + off * static_cast<size_t>(Nq);
+    rc = launch_forward(qd, kd, vd, od, ld, sub, causal, scale, 1, key_tiles(Nk), nullptr, nullptr,
+                        hp.compute);
+    if (rc != FA2_OK) break;
+    ok = cudaEventRecord(hp.computed[c], hp.compute) == cudaSuccess &&
+         cudaStreamWaitEvent(hp.out, hp.computed[c], 0) == cudaSuccess &&
+         cudaMemcpyAsync(Oh + off * q_head, od, nh * q_head * 4, cudaMemcpyDefault, hp.out) == cudaSuccess &&
+         cudaMemcpyAsync(LSEh + off * Nq, ld, nh * static_cast<size_t>(Nq) * 4, cudaMemcpyDefault,
+                         hp.out) == cudaSuccess;
+  }
+  // Join: the caller's stream continues after everything enqueued above
+  // (the copies out follow every computation, which follow every copy in).
+  const bool joined = cudaEventRecord(hp.done, hp.out) == cudaSuccess &&
+                      cudaStreamWaitEvent(s, hp.done, 0) == cudaSuccess;
+  if (rc != FA2_OK) return rc;
+  if (!ok || !joined) {
+    cudaGetLastError();
+    return FA2_ERR_LAUNCH;
+  }
+  return FA2_OK;
 }

@@ -76,9 +76,13 @@ WORKLOADS = [
 # Further measured shapes beyond the five: a long causal sequence at head
 # dimension 256 (the largest head size in the arithmetic-intensity table of
 # "Flash Attention 全解析(上)", section 1), with the same FLOP count as the
-# 16384-length d=128 case.
+# 16384-length d=128 case, and a long non-causal sequence at d=128.
 EXTRA_WORKLOADS = [
     Workload("b1_h16_n16384_d256_causal", 1, 16, 16384, 16384, 256, True, seed=6),
+    # the non-causal counterpart of the 16384-length causal case (B=1, H=32,
+    # d=128, the shape of the utilisation table in "FlashAttention-2 算法架构升级",
+    # section 四)
+    Workload("b1_h32_n16384_d128", 1, 32, 16384, 16384, 128, False, v_dist="uniform", seed=7),
 ]
 
 

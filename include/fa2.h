@@ -134,6 +134,23 @@ int fa2_forward_splitkv(const void *Q, const void *K, const void *V, float *O, f
                         void *workspace, size_t workspace_size, fa2_stream_t stream);
 
 /*
+ * Split count for fa2_forward_splitkv: the number of key ranges that fills
+ * the GPU best when the (b, h, query block) grid alone would leave SMs idle
+ * ("Flash Attention 全解析(上)" section 4: Flash Decoding splits the keys
+ * when batch x heads x query blocks cannot occupy every SM).  When the
+ * grid of 128-row query blocks is smaller than one wave (two such CTAs per
+ * SM), it estimates the run time of each count from 1 to
+ * min(64, ceil(Nk / 128)) as waves of CTAs times (key tiles per CTA + 1) and
+ * returns the smallest count with the least estimate; 1 when the grid
+ * already fills the GPU or the problem is empty.
+ *   B, H, Nq, Nk  the problem's sizes (negative sizes give 1)
+ *   sm_count      SMs of the target GPU; <= 0 queries the current device
+ *                 (1 is returned if that query fails)
+ * Host arithmetic only apart from that query; launches nothing.
+ */
+int fa2_splitkv_recommended_splits(int B, int H, int Nq, int Nk, int sm_count);
+
+/*
  * Merge of attention results computed over disjoint key subsets: the
  * ring-attention merge of "FlashAttention 怎么做?online softmax 怎么更新?"
  * (two parts) and the reduction step of Flash Decoding (many parts).  Part p
@@ -178,6 +195,37 @@ int fa2_merge(const float *O_parts, const float *LSE_parts, int num_parts, long 
 int fa2_forward_splitkv_static(const void *Q, const void *K, const void *V, float *O, float *LSE,
                                int B, int H, int Nq, int Nk, int d, int causal, float scale,
                                int num_splits, fa2_stream_t stream);
+
+/*
+ * fa2_forward with the inputs and outputs in host memory.  Q, K and V are
+ * copied into caller-owned device buffers, the forward pass runs, and O and
+ * LSE are copied back, in `chunks` groups of consecutive (b, h) heads: the
+ * copies in of one group, the computation of another and the copies out of
+ * a third run at the same time on three streams of the library's own
+ * (created by the first call on a device and kept until the process exits,
+ * together with their events).  The result is that of fa2_forward; the
+ * heads are independent, so no group needs another's data.
+ *   Qh, Kh, Vh       host (or any CUDA-addressable) bf16 inputs, layouts as
+ *                    above; page-locked memory lets the copies overlap the
+ *                    computation, pageable memory gives the same results
+ *   Oh, LSEh         host fp32 outputs, fully overwritten
+ *   Qd, Kd, Vd, Od, LSEd  device buffers of the full sizes, caller-owned,
+ *                    checked as fa2_forward checks its pointers; on return
+ *                    they hold the inputs and outputs
+ *   chunks           1..16 groups of heads (more than B*H acts as B*H)
+ *   stream           the whole call is asynchronous and ordered on `stream`:
+ *                    the copies in start after the work queued on `stream`
+ *                    before the call, and work queued on `stream` after it
+ *                    starts once every copy out has completed; synchronise
+ *                    `stream` before reading Oh and LSEh
+ * Errors as fa2_forward, plus FA2_ERR_SHAPE for `chunks` out of range and
+ * FA2_ERR_NULL for a null host pointer.  Calls on one device are enqueued
+ * one at a time (a lock), but the library's streams are shared: concurrent
+ * calls run one after another on the GPU.
+ */
+int fa2_forward_host(const void *Qh, const void *Kh, const void *Vh, float *Oh, float *LSEh,
+                     void *Qd, void *Kd, void *Vd, float *Od, float *LSEd, int B, int H, int Nq,
+                     int Nk, int d, int causal, float scale, int chunks, fa2_stream_t stream);
 
 /*
  * Bytes of device workspace fa2_backward needs: 2 * (B*H * ceil(Nq/128)*128 *

@@ -209,3 +209,39 @@ def test_typed_backward_rejects_bad_element_types_on_the_host(lib):
     # valid type, empty problem: nothing launched
     empty = [16] * 9 + [0, 1, 8, 8, 64, 0, 0.125]
     assert fa2.fa2_backward_typed(*empty, fa2.FA2_DTYPE_FP16, 256, 1 << 20, None) == fa2.FA2_OK
+
+
+def test_recommended_splits_fill_the_gpu(lib):
+    """Host arithmetic with a given SM count (152 on GB300)."""
+    rec = fa2.fa2_splitkv_recommended_splits
+    # grids that already fill the GPU keep one key range
+    assert rec(1, 32, 16384, 16384, 152) == 1
+    assert rec(4, 16, 4096, 4096, 152) == 1
+    assert rec(16, 32, 128, 8192, 152) == 1
+    # 2 x 8 heads x 8 query blocks = 128 CTAs on 304 slots: two ranges of four key tiles
+    assert rec(2, 8, 1000, 1000, 152) == 2
+    # one query row per head, 16 heads, 64 key tiles: ranges of four tiles fill one wave
+    assert rec(2, 8, 1, 8192, 152) == 16
+    # never more ranges than key tiles, never more than 64
+    assert rec(1, 1, 1, 100, 152) == 1
+    assert 1 <= rec(1, 1, 1, 1 << 20, 152) <= 64
+    # empty and invalid problems
+    assert rec(0, 8, 1000, 1000, 152) == 1
+    assert rec(1, 1, 0, 1000, 152) == 1
+    assert rec(-1, 1, 10, 10, 152) == 1
+
+
+def test_host_buffer_entry_point_checks_on_the_host(lib):
+    def c(chunks=4, B=1, **kw):
+        a = dict(Qh=16, Kh=16, Vh=16, Oh=16, Lh=16, Qd=16, Kd=16, Vd=16, Od=16, Ld=16)
+        a.update(kw)
+        return fa2.fa2_forward_host(a["Qh"], a["Kh"], a["Vh"], a["Oh"], a["Lh"], a["Qd"], a["Kd"], a["Vd"],
+                                    a["Od"], a["Ld"], B, 2, 8, 8, 64, 0, 0.125, chunks, None)
+
+    for n in (0, -3, 17):
+        assert c(chunks=n) == fa2.FA2_ERR_SHAPE
+    # empty problem: nothing copied or launched
+    assert c(B=0, Qh=None) == fa2.FA2_OK
+    # the device buffers are checked like fa2_forward's pointers
+    assert c(Qd=None) == fa2.FA2_ERR_NULL
+    assert c(Od=24) == fa2.FA2_ERR_ALIGN

@@ -2,11 +2,23 @@
 
 The GPU's forward pass produces O and LSE; the backward pass then gives dQ,
 dK and dV for a seeded upstream gradient dO.  The oracle computes the exact
-gradients of the attention definition from the same bf16 inputs, together
-with per-element magnitudes M (see oracle/attn_ref.c): the GPU rounds P and
-dS to bf16 (2^-9 relative per term) and takes D_i from the forward's O,
-whose weights carried the same rounding, so every element is within
-2^-8 M of the exact value.  The test allows 2^-7 M + 1e-6.
+gradients of the attention definition from the same inputs, together with
+per-element magnitudes M (see oracle/attn_ref.c; pinned to their
+definitions in tests/test_oracle_backward.py).
+
+Bound for bf16 inputs.  The kernel rounds P (for dV) and dS (for dQ, dK) to
+bf16, whose unit roundoff is u = 2^-8 (8-bit significand, round to nearest
+even), and takes D_i = dO_i . O_i from the forward's O, whose weights carry
+the same rounding, so D_i is off by at most u A_i.  To first order every
+element is then within u M of the exact gradient.  The remaining error comes
+from fp32 arithmetic: the recomputed scores (d products summed in fp32),
+the forward's LSE, ex2.approx, the fp32 sums of dP, D and the dQ
+reductions; each moves an element by well under 2^-13 M.  The test allows
+(2^-8 + 2^-10) M + 1e-6.
+
+Bound for fp16 inputs.  u = 2^-11, but P and dS values below fp16's normal
+range (2^-14) are rounded with an absolute error of up to 2^-25 instead of a
+relative one, which M does not cover; the test allows 2^-7 M + 1e-6 there.
 """
 import math
 
@@ -20,7 +32,7 @@ from exact_attention_17_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
-REL = 2.0 ** -7
+REL = {"bf16": 2.0 ** -8 + 2.0 ** -10, "fp16": 2.0 ** -7}
 ABS = 1e-6
 
 
@@ -47,9 +59,11 @@ def check(oracle_mod, Q, K, V, dO, causal, scale, got, heads=None, dtype="bf16")
     for name, g, r, m in zip(("dQ", "dK", "dV"), got, ref[:3], ref[3:]):
         g = g.reshape(B * H, *g.shape[2:])[hl]
         err = np.abs(g - r)
-        bound = REL * m + ABS
+        bound = REL[dtype] * m + ABS
         worst = np.max(err - bound)
-        assert worst <= 0, f"{name}: error exceeds the bound by {worst:.3e} (max err {err.max():.3e})"
+        ratio = float(np.max(err / (m + ABS / REL[dtype])))
+        assert worst <= 0, (f"{name}: error exceeds the bound by {worst:.3e} (max err {err.max():.3e}, "
+                            f"max err / M {ratio:.3e})")
         # the bound is not vacuous: the result tracks the exact gradient closely overall
         assert np.linalg.norm(g - r) <= 1e-2 * max(np.linalg.norm(r), 1e-30), name
 
@@ -111,10 +125,12 @@ def test_repeated_calls_reset_the_dq_accumulator(oracle_mod):
     assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][2], outs[1][2])
 
 
-@pytest.mark.parametrize("name,heads", [("b4_h16_n4096_d128_causal", [0, 37, 63]),
-                                        ("b1_h32_n16384_d128_causal", [5])])
-def test_backward_full_size_sampled_heads(oracle_mod, name, heads):
-    """The full workloads, every head on the GPU; sampled heads against the oracle."""
+@pytest.mark.parametrize("name,heads", [("b4_h16_n4096_d128_causal", None),
+                                        ("b1_h32_n16384_d128_causal", [0, 5, 9, 14, 18, 23, 27, 31])])
+def test_backward_full_size(oracle_mod, name, heads):
+    """The full workloads, every head on the GPU; against the oracle every head
+    of the 4096-length workload and eight of the 32 heads of the 16384-length
+    one (about 5 s of oracle time per head there)."""
     w = inputs.workload(name)
     Q, K, V = inputs.workload_inputs(w)
     dO = inputs.draw_bf16((w.B, w.H, w.Nq, w.d), w.seed, 3)
@@ -136,7 +152,7 @@ FP16 = [
 @pytest.mark.parametrize("B,H,Nq,Nk,d,causal", FP16)
 def test_backward_fp16_matches_oracle(oracle_mod, B, H, Nq, Nk, d, causal):
     """fp16 Q, K, V and dO (fa2_backward_typed): P and dS are rounded to fp16
-    (2^-11 relative per term), inside the same 2^-7 M bound."""
+    (2^-11 relative per term, or 2^-25 absolute below fp16's normal range)."""
     seed = 300 + Nq + 3 * Nk + d + int(causal)
     Q, K, V = inputs.make_qkv(B, H, Nq, Nk, d, seed, qk_std=1.5, dtype=torch.float16)
     dO = inputs.draw_bf16((B, H, Nq, d), seed, 3, dtype=torch.float16)

@@ -145,8 +145,51 @@ def check_fp16(orc):
     assert np.max(np.abs(dV - flat(v.grad.numpy()))) < 1e-12
 
 
+def magnitudes_from_definition(Qb, Kb, Vb, dOb, causal, scale):
+    """The magnitudes M_dQ, M_dK, M_dV recomputed from their definitions in
+    torch float64, sharing nothing with the oracle's C code: the weights p
+    come from torch's softmax, ds = dL/ds from torch's autograd through that
+    softmax (L = sum(O * dO)), and A_i = sum_j p_ij sum_c |dO_ic| |v_jc|.
+        M_dV = p^T |dO|
+        M_dQ = scale (|ds| + p A) |K|
+        M_dK = scale (|ds| + p A)^T |Q|"""
+    q, k, v, g = (torch.from_numpy(from_bits(x)) for x in (Qb, Kb, Vb, dOb))
+    sc = float(np.float64(np.float32(scale)))
+    s = (sc * q @ k.transpose(-1, -2)).requires_grad_(True)
+    if causal:
+        s_masked = s.masked_fill(~causal_keep(q.shape[2], k.shape[2]), float("-inf"))
+    else:
+        s_masked = s
+    p = torch.softmax(s_masked, dim=-1)
+    (p @ v * g).sum().backward()
+    ds = s.grad.abs()
+    p = p.detach()
+    A = (p * (g.abs() @ v.abs().transpose(-1, -2))).sum(-1, keepdim=True)
+    w = ds + p * A
+    mq = sc * w @ k.abs()
+    mk = sc * w.transpose(-1, -2) @ q.abs()
+    mv = p.transpose(-1, -2) @ g.abs()
+    return flat(mq.numpy()), flat(mk.numpy()), flat(mv.numpy())
+
+
+def check_magnitudes(orc):
+    """The per-element magnitudes that set the GPU tests' gradient bound equal
+    their definitions (an independent recomputation), so that a magnitude
+    that is too large -- which would loosen the GPU bound silently -- fails
+    here."""
+    rng = np.random.default_rng(26)
+    for (B, H, Nq, Nk, d, causal, scale) in [(1, 2, 6, 9, 8, False, 0.35), (2, 1, 9, 9, 16, True, 0.3),
+                                             (1, 1, 12, 5, 4, True, 0.6), (1, 1, 4, 11, 8, True, 0.25)]:
+        Q, K, V, G = (rand_bits(rng, sh) for sh in ((B, H, Nq, d), (B, H, Nk, d), (B, H, Nk, d), (B, H, Nq, d)))
+        _, _, _, mQ, mK, mV = orc.attention_backward(Q, K, V, G, causal, scale, magnitudes=True)
+        rq, rk, rv = magnitudes_from_definition(Q, K, V, G, causal, scale)
+        for got, ref in ((mQ, rq), (mK, rk), (mV, rv)):
+            assert got.shape == ref.shape
+            assert np.all(np.abs(got - ref) <= 1e-12 * np.maximum(np.abs(ref), 1e-300) + 1e-300)
+
+
 CHECKS = (check_against_autograd, check_against_central_differences, check_closed_forms,
-          check_invariants, check_fp16)
+          check_invariants, check_fp16, check_magnitudes)
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=[c.__name__ for c in CHECKS])
@@ -188,6 +231,15 @@ MUTANTS = {
     "weights_without_scale": ("const double p = exp(J->scale * acc - J->LSE[i]);",
                               "const double p = exp(acc - J->LSE[i]);"),
     "row_term_in_key_pass": ("const double ds = p * (gv - J->Dr[i]);", "const double ds = p * gv;"),
+    # mistakes that only inflate the magnitudes M (and so would loosen the GPU bound)
+    "magnitude_A_doubled": ("A += exp(s[j] - lse) * da[j];", "A += 2.0 * exp(s[j] - lse) * da[j];"),
+    "magnitude_ds_doubled_in_query_pass": ("const double w = fabs(ds) + exp(s[j] - lse) * A;",
+                                           "const double w = 2.0 * fabs(ds) + exp(s[j] - lse) * A;"),
+    "magnitude_A_doubled_in_key_pass": ("const double w = fabs(ds) + p * J->Ar[i];",
+                                        "const double w = fabs(ds) + 2.0 * p * J->Ar[i];"),
+    "magnitude_dQ_without_scale": ("mq[c] += J->scale * w * fabs(kc);", "mq[c] += w * fabs(kc);"),
+    "magnitude_dK_without_scale": ("mk[c] += J->scale * w * fabs(qc);", "mk[c] += w * fabs(qc);"),
+    "magnitude_dV_without_weights": ("mv[c] += p * fabs(gc);", "mv[c] += fabs(gc);"),
 }
 
 

@@ -1,10 +1,10 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle.
 
 Tolerances are the contract's: max |O - O_ref| <= 2e-2 and
-max |LSE - LSE_ref| <= 1e-2 on identical seeded bf16 inputs.  The two
-one-tile and ragged workloads are compared on every row; the three large
-ones at full size on sampled rows (first and last rows of tiles, the ragged
-end, random rows) plus bounds that hold for every row.
+max |LSE - LSE_ref| <= 1e-2 on identical seeded bf16 inputs.  All five
+workloads are compared on every row at full size (the oracle needs about a
+minute of host time for the 16384-length one); the large ones are also
+checked against bounds that hold for every row.
 """
 import math
 
@@ -77,22 +77,20 @@ def test_small_workloads_every_row(dev, idx):
 
 
 @pytest.mark.parametrize("idx", [2, 3, 4])
-def test_large_workloads_sampled_rows(dev, idx):
+def test_large_workloads_every_row(dev, idx):
     w = inputs.WORKLOADS[idx]
     Q, K, V = inputs.workload_inputs(w)
     O, L = gpu_forward(dev, Q, K, V, w.causal, w.scale)
-    rows = sample_rows(w.B, w.H, w.Nq, seed=idx)
-    Or, Lr = oracle.attention_rows(*bits(Q, K, V), w.causal, w.scale, rows)
-    Of = O.reshape(-1, w.d)[torch.as_tensor(rows, device=dev)]
-    Lf = L.reshape(-1)[torch.as_tensor(rows, device=dev)]
-    assert_close(Of, Lf, Or, Lr, w.name)
     # every row: finite, and each O row inside the per-head range of V
     assert bool(torch.isfinite(O).all()) and bool(torch.isfinite(L).all())
     Vd = V.to(dev).float()
     vmin = Vd.amin(dim=2, keepdim=True)
     vmax = Vd.amax(dim=2, keepdim=True)
     assert bool((O >= vmin - 1e-3).all()) and bool((O <= vmax + 1e-3).all())
-    del O, L, Vd
+    del Vd
+    O, L = O.cpu(), L.cpu()
+    Or, Lr = oracle.attention(*bits(Q, K, V), w.causal, w.scale)
+    assert_close(O, L, Or, Lr, w.name)
 
 
 # ---------------------------------------------------------------- edge cases

@@ -599,3 +599,47 @@ def test_model_catches_early_rearm():
         except ProtocolError:
             failures += 1
     assert failures > 0
+
+
+def test_model_catches_commits_from_another_lane_than_the_mmas():
+    """tcgen05.commit makes its mbarrier track only the tensor-core operations
+    issued by the thread that executes it.  The kernel issues every MMA and
+    every commit from one thread (lane 0 of the MMA warp).  A variant that
+    picks the issuing lane afresh for each group of MMAs and for each commit
+    (the PTX description of elect.sync does not promise which active lane it
+    elects) can issue a commit from a lane that issued none of the MMAs it
+    is meant to cover: its arrival then does not wait for them, and the
+    softmax or the epilogue reads TMEM before the MMA has written it --
+    wrong values, with no fault and no timed-out wait.  The model must
+    reject that variant."""
+    class LaneSwitching(Sim):
+        def mma(self, reads, tmem=None):
+            self.current = ("issuer", self.rng.randrange(2))
+            super().mma(reads, tmem)
+
+        def commit(self, bar, release=None):
+            self.current = ("issuer", self.rng.randrange(2))
+            super().commit(bar, release)
+
+    failures = 0
+    for seed in range(200):
+        try:
+            LaneSwitching(4, 5, 5, seed).run()
+        except ProtocolError:
+            failures += 1
+    assert failures > 0
+
+
+def test_one_issuing_lane_passes_the_same_interleavings():
+    """The same seeds with every MMA and commit from one lane are clean."""
+    class OneLane(Sim):
+        def mma(self, reads, tmem=None):
+            self.current = ("issuer", 0)
+            super().mma(reads, tmem)
+
+        def commit(self, bar, release=None):
+            self.current = ("issuer", 0)
+            super().commit(bar, release)
+
+    for seed in range(200):
+        OneLane(4, 5, 5, seed).run()
