@@ -163,15 +163,47 @@ def fa2_check_wait_timeout(timeout_ns: int, stream=None) -> int:
 
 
 def _stream_handle(stream):
-    import torch
-
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    handle = getattr(stream, "cuda_stream", None)
+    return stream if handle is None else handle
+
+
+_DTYPE_CODES = None
+
+
+def _dtype_codes():
+    global _DTYPE_CODES
+    if _DTYPE_CODES is None:
+        import torch
+
+        _DTYPE_CODES = {torch.bfloat16: FA2_DTYPE_BF16, torch.float16: FA2_DTYPE_FP16,
+                        torch.float32: FA2_DTYPE_FP32}
+    return _DTYPE_CODES
+
+
+class _on_device:
+    """Make `device` current for the call, only when it is not already (the
+    switch costs microseconds a small problem does not have)."""
+
+    def __init__(self, device):
+        import torch
+
+        self.ctx = None if device.index == torch.cuda.current_device() else torch.cuda.device(device)
+
+    def __enter__(self):
+        if self.ctx is not None:
+            self.ctx.__enter__()
+
+    def __exit__(self, *exc):
+        if self.ctx is not None:
+            self.ctx.__exit__(*exc)
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-            stream=None, impl: str = "tc", num_splits: int = 1, workspace=None, out_dtype=None):
+            stream=None, impl: str = "tc", num_splits=1, workspace=None, out_dtype=None):
     """Attention forward on torch CUDA tensors.
 
     q: [B,H,Nq,d]; k, v: [B,H,Nk,d]; all bf16 or all fp16, contiguous, on one
@@ -186,54 +218,60 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     """
     import torch
 
+    codes = _dtype_codes()
     in_dtype = q.dtype
-    if in_dtype not in (torch.bfloat16, torch.float16):
+    if in_dtype is not torch.bfloat16 and in_dtype is not torch.float16:
         raise ValueError("q must be bf16 or fp16")
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != in_dtype or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+        if t.dtype is not in_dtype or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor of q's dtype")
     out_dtype = torch.float32 if out_dtype is None else out_dtype
-    if out_dtype not in (torch.float32, in_dtype):
+    if out_dtype is not torch.float32 and out_dtype is not in_dtype:
         raise ValueError("out_dtype must be fp32 or the input dtype")
-    typed = in_dtype != torch.bfloat16 or out_dtype != torch.float32
+    typed = in_dtype is not torch.bfloat16 or out_dtype is not torch.float32
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
-    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+    if k.shape != (B, H, Nk, d) or v.shape != (B, H, Nk, d):
         raise ValueError("k and v must be [B, H, Nk, d] matching q")
     if scale is None:
         scale = float(torch.tensor(d, dtype=torch.float64).rsqrt().float())
+    device = q.device
     if out is None:
-        out = torch.empty((B, H, Nq, d), dtype=out_dtype, device=q.device)
+        out = torch.empty((B, H, Nq, d), dtype=out_dtype, device=device)
     if lse is None:
-        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    for name, t, shape, dt in (("out", out, (B, H, Nq, d), out_dtype), ("lse", lse, (B, H, Nq), torch.float32)):
-        if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
-            raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shape} on {q.device}")
-    if num_splits == "auto":
-        with torch.cuda.device(q.device):
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=device)
+    if (out.dtype is not out_dtype or out.shape != (B, H, Nq, d) or not out.is_contiguous()
+            or out.device != device):
+        raise ValueError(f"out must be a contiguous {out_dtype} tensor of shape {(B, H, Nq, d)} on {device}")
+    if lse.dtype is not torch.float32 or lse.shape != (B, H, Nq) or not lse.is_contiguous() or lse.device != device:
+        raise ValueError(f"lse must be a contiguous fp32 tensor of shape {(B, H, Nq)} on {device}")
+    with _on_device(device):
+        if num_splits == "auto":
             num_splits = fa2_splitkv_recommended_splits(B, H, Nq, Nk, 0)
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-            B, H, Nq, Nk, d, causal, float(scale))
-    codes = {torch.bfloat16: FA2_DTYPE_BF16, torch.float16: FA2_DTYPE_FP16, torch.float32: FA2_DTYPE_FP32}
-    with torch.cuda.device(q.device):
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                B, H, Nq, Nk, d, causal, float(scale))
+        sh = _stream_handle(stream)
         if typed:
             if impl != "tc" or num_splits > 1:
                 raise ValueError("fp16 inputs and 16-bit outputs run on the single-pass tensor-core path")
-            rc = fa2_forward_typed(*args, codes[in_dtype], codes[out_dtype], _stream_handle(stream))
+            rc = fa2_forward_typed(*args, codes[in_dtype], codes[out_dtype], sh)
             name = "fa2_forward_typed"
         elif num_splits > 1:
             if impl != "tc":
                 raise ValueError("split-KV runs on the tensor-core path only")
             need = fa2_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
             if workspace is None:
-                workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-            rc = fa2_forward_splitkv(*args, num_splits, workspace.data_ptr(), workspace.numel(),
-                                     _stream_handle(stream))
+                workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+            rc = fa2_forward_splitkv(*args, num_splits, workspace.data_ptr(), workspace.numel(), sh)
             name = "fa2_forward_splitkv"
+        elif impl == "tc":
+            rc = fa2_forward(*args, sh)
+            name = "fa2_forward"
+        elif impl == "simt":
+            rc = fa2_forward_simt(*args, sh)
+            name = "fa2_forward_simt"
         else:
-            fn = {"tc": fa2_forward, "simt": fa2_forward_simt}[impl]
-            rc = fn(*args, _stream_handle(stream))
-            name = "fa2_forward" if impl == "tc" else "fa2_forward_simt"
+            raise ValueError(f"unknown impl {impl!r}")
     if rc != FA2_OK:
         raise FA2Error(rc, name)
     return out, lse

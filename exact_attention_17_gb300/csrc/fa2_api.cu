@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -69,7 +70,8 @@ int device_ready() {
     if (fa2host::prepare_tc_d64_bf16() != cudaSuccess || fa2host::prepare_tc_d128_bf16() != cudaSuccess ||
         fa2host::prepare_tc_d64_f16() != cudaSuccess || fa2host::prepare_tc_d128_f16() != cudaSuccess ||
         fa2host::prepare_tc_d256_bf16() != cudaSuccess || fa2host::prepare_tc_d256_f16() != cudaSuccess ||
-        fa2host::prepare_simt() != cudaSuccess || fa2host::prepare_bwd() != cudaSuccess)
+        fa2host::prepare_tc_pair_d128() != cudaSuccess || fa2host::prepare_simt() != cudaSuccess ||
+        fa2host::prepare_bwd() != cudaSuccess)
       return;
     st.usable = true;
   });
@@ -158,13 +160,14 @@ int* status_word() {
 }
 
 // 3-D map over [BH][N][d] 16-bit elements (bf16 or fp16): box = 64 columns
-// (128 B, one swizzle atom) x 128 rows x 1.  Rows past N read as zero
-// instead of running into the next head.
-bool encode_map(CUtensorMap* map, const void* base, int d, int N, int BH, bool f16) {
+// (128 B, one swizzle atom) x `rows` rows x 1 (128 by default; 64 for the
+// K halves of the two-SM kernel).  Rows past N read as zero instead of
+// running into the next head.
+bool encode_map(CUtensorMap* map, const void* base, int d, int N, int BH, bool f16, unsigned rows = 128) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = driver().encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                3, const_cast<void*>(base), dims,
@@ -259,6 +262,10 @@ int validate(const void* Q, const void* K, const void* V, const void* O, const f
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// The two-SM kernel is the default for the shapes where the one-CTA kernel
+// takes two query sub-tiles per CTA.
+constexpr bool kPairByDefault = false;
+
 // Query sub-tiles of 128 rows per CTA.  Two (one CTA per SM, the sub-tiles
 // ping-pong on the tensor core) is faster for long query blocks; one (two
 // CTAs per SM) when a second sub-tile would have no rows (Nq <= 128) or when
@@ -282,6 +289,19 @@ int item_group(const Problem& pr, int splits) {
   return static_cast<int>(g);
 }
 
+// Which forward kernel runs a head-dimension-128 problem: the two-SM kernel
+// (a CTA pair per 512 query rows) or the one-CTA kernel.  FA2_FORWARD_KERNEL
+// = "pair" or "single" in the environment overrides the choice (for
+// comparing the two); by default the pair kernel runs where the one-CTA
+// kernel would take two query sub-tiles per CTA.
+bool use_pair_kernel(const Problem& pr, int subs) {
+  if (pr.d != 128) return false;
+  const char* v = std::getenv("FA2_FORWARD_KERNEL");
+  if (v != nullptr && std::strcmp(v, "pair") == 0) return true;
+  if (v != nullptr && std::strcmp(v, "single") == 0) return false;
+  return kPairByDefault && subs == 2;
+}
+
 // Launch of the tensor-core kernel over `splits` key ranges of `tiles_per_split`
 // tiles each (splits == 1: the whole key range, outputs O and LSE directly).
 int launch_forward(const void* Q, const void* K, const void* V, float* O, float* LSE,
@@ -290,13 +310,16 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
                    bool o_half = false) {
   const int Nq = pr.Nq, Nk = pr.Nk, d = pr.d;
   const int subs = subtiles_per_cta(pr, splits);
-  const long long blocks = (static_cast<long long>(Nq) + 128 * subs - 1) / (128 * subs);
-  if (blocks * pr.BH * splits > 0x7fffffffLL) return FA2_ERR_SHAPE;
+  const bool pair = use_pair_kernel(pr, subs);
+  // query blocks: 512 rows per CTA pair, else 128 x subs rows per CTA
+  const long long rows_per_block = pair ? 512 : 128 * subs;
+  const long long blocks = (static_cast<long long>(Nq) + rows_per_block - 1) / rows_per_block;
+  if (blocks * pr.BH * splits * (pair ? 2 : 1) > 0x7fffffffLL) return FA2_ERR_SHAPE;
 
   CUtensorMap mq, mk, mv, mo;
   const bool split_out = splits > 1;
   if (!encode_map(&mq, Q, d, Nq, static_cast<int>(pr.BH), f16) ||
-      !encode_map(&mk, K, d, Nk, static_cast<int>(pr.BH), f16) ||
+      !encode_map(&mk, K, d, Nk, static_cast<int>(pr.BH), f16, pair ? 64 : 128) ||
       !encode_map(&mv, V, d, Nk, static_cast<int>(pr.BH), f16) ||
       !encode_map_out(&mo, split_out ? static_cast<const void*>(O_part) : static_cast<const void*>(O), d, Nq,
                       split_out ? pr.BH * splits : pr.BH, (o_half && !split_out) ? 2 : 4, f16))
@@ -320,14 +343,16 @@ int launch_forward(const void* Q, const void* K, const void* V, float* O, float*
   p.div_per_group = make_fast_div(static_cast<int>(p.item_group * blocks));
   p.div_group = make_fast_div(p.item_group);
   p.div_splits = make_fast_div(splits);
-  p.wave = sm_count() * (subs == 2 || d == 256 ? 1 : 2);
+  p.wave = sm_count() * (pair || subs == 2 || d == 256 ? 1 : 2);
   p.status = status_word();
   if (p.status == nullptr) return FA2_ERR_LAUNCH;
 
-  const unsigned grid = static_cast<unsigned>(blocks * pr.BH * splits);
+  const unsigned grid = static_cast<unsigned>(blocks * pr.BH * splits * (pair ? 2 : 1));
   const bool c = causal != 0;
   cudaError_t e;
-  if (d == 64)
+  if (pair)
+    e = fa2host::launch_tc_pair_d128(c, f16, mq, mk, mv, mo, p, grid, s);
+  else if (d == 64)
     e = f16 ? fa2host::launch_tc_d64_f16(subs, c, mq, mk, mv, mo, p, grid, s)
             : fa2host::launch_tc_d64_bf16(subs, c, mq, mk, mv, mo, p, grid, s);
   else if (d == 128)

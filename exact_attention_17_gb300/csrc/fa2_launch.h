@@ -7,6 +7,7 @@
 
 #include "fa2_bwd_sm103.cuh"
 #include "fa2_fwd_simt.cuh"
+#include "fa2_fwd_pair_sm103.cuh"
 #include "fa2_fwd_sm103.cuh"
 
 namespace fa2host {
@@ -34,6 +35,13 @@ FA2_DECLARE_TC_LAUNCH(launch_tc_d256_bf16)
 FA2_DECLARE_TC_LAUNCH(launch_tc_d256_f16)
 #undef FA2_DECLARE_TC_LAUNCH
 cudaError_t launch_simt(int d, bool causal, const fa2dev::SimtParams& p, dim3 grid, cudaStream_t s);
+
+// Two-SM forward (clusters of two CTAs), head dimension 128.  mk_half: K with
+// 64-row boxes; mq, mv: 128-row boxes.  grid: an even number of CTAs.
+cudaError_t prepare_tc_pair_d128();
+cudaError_t launch_tc_pair_d128(bool causal, bool f16, const CUtensorMap& mq, const CUtensorMap& mk_half,
+                                const CUtensorMap& mv, const CUtensorMap& mo, const fa2dev::FwdParams& p,
+                                unsigned grid, cudaStream_t s);
 
 // Merge of S partial results (normalised O [S, R, d], LSE [S, R]) into O [R, d], LSE [R].
 cudaError_t launch_combine(int d, const float* O_part, const float* LSE_part, int S, long long R,
