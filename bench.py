@@ -407,7 +407,7 @@ def main():
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count (smaller profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunks", type=int, default=4,
+    ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="groups of heads the end-to-end call pipelines its copies over")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other workloads measured beside the headline one")

@@ -349,11 +349,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (possibly in
-// another CTA of the cluster), releasing this thread's prior writes at
-// cluster scope.
+// Arrive on an mbarrier given by its shared::cluster address (in another
+// CTA of the cluster), relaxed: no fence before the arrival.  A release at
+// cluster scope fences all of the thread's memory operations across the
+// cluster first, a membar of hundreds of cycles on the path the arrival
+// sits on.  The callers arrive only once what the other CTA relies on is
+// already complete: their own TMEM stores (after tcgen05.wait::st and
+// tcgen05.fence::before_thread_sync), or copies they have seen land on
+// their own barrier.
 __device__ __forceinline__ void bar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 
