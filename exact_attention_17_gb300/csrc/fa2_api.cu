@@ -425,11 +425,17 @@ namespace {
 // Split count for fa2_forward_splitkv on a machine with `sms` SMs.  Without a
 // split every (b*H + h, query block) is one CTA of one 128-row sub-tile, two
 // of which run on each SM; with S key ranges there are S times as many CTAs,
-// each visiting about 1/S of the key tiles.  The estimate of the time is
-// (waves of CTAs) x (key tiles per CTA + 1), the 1 standing for a CTA's
-// fixed start and end costs; the smallest S with the least estimate wins.
+// each visiting about 1/S of the key tiles, and a second kernel merges the
+// ranges.  The estimate of the time, in units of one key tile of one CTA,
+// is (waves of CTAs) x (key tiles per CTA + kCtaFixedTiles) plus, for S > 1,
+// kMergeTiles: measured, a CTA's start and end cost about four tiles' time
+// (a 1000-length, 16-head problem ran slower in two ranges than in one) and
+// the merge launch about five.  The smallest S with the least estimate wins.
 // Only grids that leave CTA slots empty are split: a grid of a wave or more
 // keeps S = 1.
+constexpr long long kCtaFixedTiles = 4;
+constexpr long long kMergeTiles = 5;
+
 int recommended_splits(long long BH, int Nq, int Nk, int sms) {
   if (BH <= 0 || Nq <= 0 || Nk <= 0 || sms <= 0) return 1;
   const long long ctas = (static_cast<long long>(Nq) + 127) / 128 * BH;
@@ -443,7 +449,7 @@ int recommended_splits(long long BH, int Nq, int Nk, int sms) {
     split_plan(Nk, want, &splits, &tps);
     if (splits != want) continue;   // the same plan as a smaller count
     const long long waves = (ctas * splits + slots - 1) / slots;
-    const long long cost = waves * (tps + 1);
+    const long long cost = waves * (tps + kCtaFixedTiles) + (splits > 1 ? kMergeTiles : 0);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = splits;

@@ -35,6 +35,7 @@
 #pragma once
 
 #include "fa2_fwd_sm103.cuh"
+#include "ptx_pair.cuh"
 
 namespace fa2dev {
 

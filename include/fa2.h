@@ -140,9 +140,10 @@ int fa2_forward_splitkv(const void *Q, const void *K, const void *V, float *O, f
  * when batch x heads x query blocks cannot occupy every SM).  When the
  * grid of 128-row query blocks is smaller than one wave (two such CTAs per
  * SM), it estimates the run time of each count from 1 to
- * min(64, ceil(Nk / 128)) as waves of CTAs times (key tiles per CTA + 1) and
- * returns the smallest count with the least estimate; 1 when the grid
- * already fills the GPU or the problem is empty.
+ * min(64, ceil(Nk / 128)) as waves of CTAs times (key tiles per CTA + 4,
+ * a CTA's fixed start and end cost), plus 5 tiles for the merge when the
+ * keys are split, and returns the smallest count with the least estimate;
+ * 1 when the grid already fills the GPU or the problem is empty.
  *   B, H, Nq, Nk  the problem's sizes (negative sizes give 1)
  *   sm_count      SMs of the target GPU; <= 0 queries the current device
  *                 (1 is returned if that query fails)
