@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(PKG, "libfa2.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["fa2_api.cu", "fa2_tc_d64_bf16.cu", "fa2_tc_d128_bf16.cu", "fa2_tc_d256_bf16.cu",
            "fa2_tc_d64_f16.cu", "fa2_tc_d128_f16.cu", "fa2_tc_d256_f16.cu", "fa2_simt.cu",
-           "fa2_combine.cu", "fa2_bwd.cu", "fa2_tc_pair_d128.cu"]
+           "fa2_combine.cu", "fa2_bwd.cu", "fa2_tc_pair_d128.cu", "fa2_bwd2.cu"]
 
 
 def nvcc() -> str:

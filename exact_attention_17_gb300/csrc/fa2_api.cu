@@ -71,7 +71,7 @@ int device_ready() {
         fa2host::prepare_tc_d64_f16() != cudaSuccess || fa2host::prepare_tc_d128_f16() != cudaSuccess ||
         fa2host::prepare_tc_d256_bf16() != cudaSuccess || fa2host::prepare_tc_d256_f16() != cudaSuccess ||
         fa2host::prepare_tc_pair_d128() != cudaSuccess || fa2host::prepare_simt() != cudaSuccess ||
-        fa2host::prepare_bwd() != cudaSuccess)
+        fa2host::prepare_bwd() != cudaSuccess || fa2host::prepare_bwd2() != cudaSuccess)
       return;
     st.usable = true;
   });
@@ -177,13 +177,14 @@ bool encode_map(CUtensorMap* map, const void* base, int d, int N, int BH, bool f
   return r == CUDA_SUCCESS;
 }
 
-// 3-D map over an fp32 [BH][N][d] array: box = 32 columns (128 B) x 128 rows x 1,
-// 128-byte swizzle; the backward pass adds its dQ partials through it.
-bool encode_map_f32(CUtensorMap* map, const void* base, int d, int N, int BH) {
+// 3-D map over an fp32 [BH][N][d] array: box = 32 columns (128 B) x `rows`
+// rows x 1 (128 by default; 32 for the two-tile backward kernel), 128-byte
+// swizzle; the backward pass adds its dQ partials through it.
+bool encode_map_f32(CUtensorMap* map, const void* base, int d, int N, int BH, unsigned rows = 128) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
-  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t box[3] = {32, rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = driver().encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
                                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -555,6 +556,19 @@ extern "C" size_t fa2_backward_workspace_bytes(int B, int H, int Nq) {
 
 namespace {
 
+// The two-tile backward kernel (two 64-row query tiles in flight) runs head
+// dimension 128 by default; FA2_BACKWARD_KERNEL = "one_tile" or "two_tile"
+// in the environment overrides the choice (for comparing the two).
+constexpr bool kTwoTileByDefault = false;
+
+bool use_two_tile_backward(int d) {
+  if (d != 128) return false;
+  const char* v = std::getenv("FA2_BACKWARD_KERNEL");
+  if (v != nullptr && std::strcmp(v, "two_tile") == 0) return true;
+  if (v != nullptr && std::strcmp(v, "one_tile") == 0) return false;
+  return kTwoTileByDefault;
+}
+
 // The backward pass for bf16 (f16 = false) or fp16 Q, K, V and dO.
 int backward_impl(const void* Q, const void* K, const void* V, const float* O, const void* dO,
                   const float* LSE, float* dQ, float* dK, float* dV, int B, int H, int Nq, int Nk,
@@ -597,12 +611,15 @@ int backward_impl(const void* Q, const void* K, const void* V, const float* O, c
       !device_range_ok(workspace, need))
     return FA2_ERR_MEMORY;
 
+  // the two-tile kernel (64-row query tiles) for head dimension 128
+  const bool two_tile = use_two_tile_backward(d);
+  const unsigned qrows = two_tile ? 64 : 128;
   CUtensorMap mq, mk, mv, mdo, mdq;
-  if (!encode_map(&mq, Q, d, Nq, static_cast<int>(BH), f16) ||
+  if (!encode_map(&mq, Q, d, Nq, static_cast<int>(BH), f16, qrows) ||
       !encode_map(&mk, K, d, Nk, static_cast<int>(BH), f16) ||
       !encode_map(&mv, V, d, Nk, static_cast<int>(BH), f16) ||
-      !encode_map(&mdo, dO, d, Nq, static_cast<int>(BH), f16) ||
-      !encode_map_f32(&mdq, dQ, d, Nq, static_cast<int>(BH)))
+      !encode_map(&mdo, dO, d, Nq, static_cast<int>(BH), f16, qrows) ||
+      !encode_map_f32(&mdq, dQ, d, Nq, static_cast<int>(BH), two_tile ? 32 : 128))
     return FA2_ERR_SHAPE;
 
   const int Nq_pad = (Nq + 127) / 128 * 128;
@@ -634,10 +651,10 @@ int backward_impl(const void* Q, const void* K, const void* V, const float* O, c
   if (p.status == nullptr) return FA2_ERR_LAUNCH;
   const long long grid = BH * p.key_blocks;
   if (grid > 0x7fffffffLL) return FA2_ERR_SHAPE;
-  return fa2host::launch_bwd(d, causal != 0, f16, mq, mk, mv, mdo, mdq, p, static_cast<unsigned>(grid), s) ==
-                 cudaSuccess
-             ? FA2_OK
-             : FA2_ERR_LAUNCH;
+  const cudaError_t e =
+      two_tile ? fa2host::launch_bwd2(causal != 0, f16, mq, mk, mv, mdo, mdq, p, static_cast<unsigned>(grid), s)
+               : fa2host::launch_bwd(d, causal != 0, f16, mq, mk, mv, mdo, mdq, p, static_cast<unsigned>(grid), s);
+  return e == cudaSuccess ? FA2_OK : FA2_ERR_LAUNCH;
 }
 
 }  // namespace

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa2_bwd2_sm103.cuh"
 #include "fa2_bwd_sm103.cuh"
 #include "fa2_fwd_simt.cuh"
 #include "fa2_fwd_pair_sm103.cuh"
@@ -58,5 +59,12 @@ cudaError_t launch_bwd(int d, bool causal, bool f16, const CUtensorMap& mq, cons
 cudaError_t launch_bwd_pre(int d, bool f16, const float* O, const void* dO, const float* LSE, float* dQ,
                            float* L2, float* Dr, long long rows, int Nq, int Nq_pad, cudaStream_t s);
 cudaError_t launch_zero(float* p, long long n, cudaStream_t s);
+
+// Two-tile backward kernel (fa2_bwd2.cu), head dimension 128.  mq64, mdo64:
+// 64-row boxes; mk, mv: 128-row boxes; mdq32: fp32 dQ with 32 x 32 boxes.
+cudaError_t prepare_bwd2();
+cudaError_t launch_bwd2(bool causal, bool f16, const CUtensorMap& mq64, const CUtensorMap& mk,
+                        const CUtensorMap& mv, const CUtensorMap& mdo64, const CUtensorMap& mdq32,
+                        const fa2dev::BwdParams& p, unsigned grid, cudaStream_t s);
 
 }  // namespace fa2host

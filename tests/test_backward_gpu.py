@@ -64,8 +64,10 @@ def check(oracle_mod, Q, K, V, dO, causal, scale, got, heads=None, dtype="bf16")
         ratio = float(np.max(err / (m + ABS / REL[dtype])))
         assert worst <= 0, (f"{name}: error exceeds the bound by {worst:.3e} (max err {err.max():.3e}, "
                             f"max err / M {ratio:.3e})")
-        # the bound is not vacuous: the result tracks the exact gradient closely overall
-        assert np.linalg.norm(g - r) <= 1e-2 * max(np.linalg.norm(r), 1e-30), name
+        # the bound is not vacuous: the result tracks the exact gradient closely
+        # overall (with the elementwise ABS as a floor, for gradients that are
+        # exactly zero, e.g. dQ with a single key)
+        assert np.linalg.norm(g - r) <= max(1e-2 * np.linalg.norm(r), ABS * np.sqrt(r.size)), name
 
 
 SMALL = [
