@@ -8,16 +8,19 @@
 //  * one CTA owns a block of 128 keys (K_j, V_j stay in shared memory) and
 //    streams query tiles of 64 rows (Q_i, dO_i through a TMA ring);
 //  * TMEM holds S^T and dP^T for two tiles (buffer t % 2, 64 columns each)
-//    beside the dV and dK accumulators (128 columns each): 512 columns.  So
-//    S^T(t+1) = K Q(t+1)^T and dP^T(t+1) = V dO(t+1)^T run on the tensor
-//    core while the elementwise warps turn tile t's scores into P^T and dS^T
-//    and while dV(t), dK(t) and dQ(t) run -- the one-tile kernel had to wait
-//    for each tile's dQ read-out before the next tile's scores;
+//    beside the dV and dK accumulators (128 columns each): 512 columns;
+//  * the two elementwise warpgroups take the tiles in turn: warpgroup g owns
+//    the tiles t with t % 2 == g (buffer g, its own barriers and its own dS
+//    tile in shared memory), so one warpgroup's phases -- each bound by
+//    fixed latencies (barrier waits, TMEM round trips) more than by its
+//    arithmetic -- overlap the other's, and the tensor core computes the
+//    scores of one tile while the other tile's dV, dK and dQ MMAs wait for
+//    their operands;
 //  * dQ is computed transposed, dQ^T(t) = K^T dS^T(t) (M = 128 head columns,
 //    N = 64 queries, K = 128 keys), into tile t's S^T buffer once dV(t) has
-//    read P^T(t) from it; the elementwise warps read it out (TMEM lane = head
-//    column), stage it in the finished tile's ring slot as [query][column]
-//    boxes and add it into dQ with TMA bulk reductions;
+//    read P^T(t) from it; the owning warpgroup reads it out (TMEM lane =
+//    head column), stages it in tile t's ring slot as [query][column] boxes
+//    and adds it into dQ with TMA bulk reductions;
 //  * per tile one thread issues: dV(t) after P^T(t) is written, then
 //    dP^T(t+1) and S^T(t+1) once Q/dO(t+1) have landed and dQ^T(t-1) has
 //    been read out of buffer (t+1) % 2, then dK(t) and dQ^T(t) after dS^T(t).
@@ -46,29 +49,31 @@ struct Bwd2Config {
   static constexpr uint32_t kKVChunk = 128 * 128;            // 64 columns of the 128-row block
   static constexpr uint32_t kQChunk = kQRows * 128;          // 64 columns of a 64-row tile
   static constexpr int kStages = 4;                          // Q/dO ring slots
-  static constexpr uint32_t kDsBytes = 128 * kQRows * 2;     // dS [128 keys][64 queries]
-  static constexpr uint32_t kSmemData = 2 * kKVBytes + kStages * 2 * kQBytes + kDsBytes;
+  static constexpr uint32_t kDsBytes = 128 * kQRows * 2;     // a dS tile [128 keys][64 queries]
+  static constexpr uint32_t kSmemData = 2 * kKVBytes + kStages * 2 * kQBytes + 2 * kDsBytes;
   static constexpr uint32_t kSmemBytes = kSmemData + 1024 /*align*/ + 1024 /*barriers*/;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static constexpr uint32_t kColS = 0;      // S^T buffer b at [64 b, 64 b + 64): P^T, then dQ^T
   static constexpr uint32_t kColDP = 128;   // dP^T buffer b at [128 + 64 b, +64): dS^T
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 384;
-  // a warpgroup's dQ staging (32 queries x 128 columns fp32) fills half a ring slot
+  // a tile's dQ staging (64 queries x 128 columns fp32) fills its ring slot:
+  // queries 0-31 the Q half, 32-63 the dO half
   static_assert(32 * D * 4 == kQBytes, "dQ staging in the ring slot");
 };
 
+// Index g: the warpgroup (and TMEM buffer, and dS tile) of tiles t % 2 == g.
 template <int STAGES>
 struct alignas(8) Bwd2Barriers {
   uint64_t kv_full;
   uint64_t q_full[STAGES];
-  uint64_t q_empty[STAGES];   // one arrival per warpgroup once its dQ staging was read
-  uint64_t dq_staged[2];      // per warpgroup: its 128 threads wrote their dQ columns
-  uint64_t s_full;            // S^T(t) and dP^T(t) complete
-  uint64_t p_ready;
-  uint64_t ds_ready;
-  uint64_t dq_full;
-  uint64_t dq_free;
+  uint64_t q_empty[STAGES];   // the owning warpgroup: the tile's dQ staging was read
+  uint64_t dq_staged[2];      // the warpgroup's 128 threads wrote their dQ columns
+  uint64_t s_full[2];         // S^T(t) and dP^T(t) complete
+  uint64_t p_ready[2];
+  uint64_t ds_ready[2];
+  uint64_t dq_full[2];
+  uint64_t dq_free[2];
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort;
@@ -99,7 +104,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sV = smem + KVB;
   uint8_t* sQ = smem + 2 * KVB;            // STAGES tiles
   uint8_t* sdO = sQ + STAGES * QB;         // STAGES tiles
-  uint8_t* sdS = sdO + STAGES * QB;        // [128 keys][64 queries], MN-major B of dQ^T
+  uint8_t* sdS = sdO + STAGES * QB;        // 2 tiles [128 keys][64 queries], MN-major B of dQ^T
   auto* bars = reinterpret_cast<Bwd2Barriers<STAGES>*>(smem + Cfg::kSmemData);
   volatile int* abort = &bars->abort;
 
@@ -125,15 +130,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bar_init(&bars->kv_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       bar_init(&bars->q_full[s], 1);
-      bar_init(&bars->q_empty[s], 2);
+      bar_init(&bars->q_empty[s], 1);
     }
-    bar_init(&bars->dq_staged[0], 128);
-    bar_init(&bars->dq_staged[1], 128);
-    bar_init(&bars->s_full, 1);
-    bar_init(&bars->p_ready, 256);
-    bar_init(&bars->ds_ready, 256);
-    bar_init(&bars->dq_full, 1);
-    bar_init(&bars->dq_free, 256);
+    for (int g = 0; g < 2; ++g) {
+      bar_init(&bars->dq_staged[g], 128);
+      bar_init(&bars->s_full[g], 1);
+      bar_init(&bars->p_ready[g], 128);
+      bar_init(&bars->ds_ready[g], 128);
+      bar_init(&bars->dq_full[g], 1);
+      bar_init(&bars->dq_free[g], 128);
+    }
     bar_init(&bars->mma_drain, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -202,13 +208,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             asm volatile("" : "+l"(da), "+l"(db));
           }
         };
-        // D[128 keys x D] (+)= A[tmem: 128 keys x 64 queries] B, B an MN-major
-        // 64-row tile; warpgroup w's 32 queries are packed at acol + 32 w.
+        // D[128 keys x D] (+)= A[tmem: 128 keys x 64 queries, packed two per
+        // column] B, B an MN-major 64-row tile.
         auto issue_acc = [&](uint32_t dcol, uint32_t acol, uint32_t b0, bool acc) {
           uint64_t db = sdesc_sw128(b0, Cfg::kQChunk, 1024);
 #pragma unroll
           for (int kk = 0; kk < QR / 16; ++kk) {
-            const uint32_t a = tmem + acol + 32 * (kk >> 1) + 8 * (kk & 1);
+            const uint32_t a = tmem + acol + 8 * kk;
             mma_ts(tmem + dcol, a, db, kIdAcc, (acc || kk > 0) ? 1u : 0u);
             db += 2048 >> 4;   // next 16 queries
             asm volatile("" : "+l"(db));
@@ -218,7 +224,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int slot = t % STAGES, b = t & 1;
           issue_scores(Cfg::kColDP + 64 * b, aV, adO + slot * QB);   // dP^T = V dO^T
           issue_scores(Cfg::kColS + 64 * b, aK, aQ + slot * QB);     // S^T = K Q^T
-          mma_commit(&bars->s_full);
+          mma_commit(&bars->s_full[b]);
         };
 
         bool ok = wait_bar(&bars->kv_full, 0, abort, p.timeout_ns) &&
@@ -229,22 +235,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         for (int t = 0; t < n_tiles && ok; ++t) {
           const int slot = t % STAGES, b = t & 1;
-          if (!wait_bar(&bars->p_ready, t & 1, abort, p.timeout_ns)) { ok = false; break; }
+          const uint32_t kp = (t >> 1) & 1;   // phase of tile t on its warpgroup's barriers
+          if (!wait_bar(&bars->p_ready[b], kp, abort, p.timeout_ns)) { ok = false; break; }
           tc_fence_after_sync();
           issue_acc(Cfg::kColDV, Cfg::kColS + 64 * b, adO + slot * QB, t > 0);     // dV += P^T dO
           if (t + 1 < n_tiles) {
             const int s1 = (t + 1) % STAGES;
             if (!wait_bar(&bars->q_full[s1], ((t + 1) / STAGES) & 1, abort, p.timeout_ns)) { ok = false; break; }
-            // buffer (t+1) % 2 holds dQ^T(t-1) until it has been read out
-            if (t >= 1 && !wait_bar(&bars->dq_free, (t - 1) & 1, abort, p.timeout_ns)) { ok = false; break; }
+            // buffer (t+1) % 2 holds dQ^T(t-1) until its warpgroup has read it out
+            if (t >= 1 && !wait_bar(&bars->dq_free[b ^ 1], ((t - 1) >> 1) & 1, abort, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
             tc_fence_after_sync();
             issue_sp(t + 1);
           }
-          if (!wait_bar(&bars->ds_ready, t & 1, abort, p.timeout_ns)) { ok = false; break; }
+          if (!wait_bar(&bars->ds_ready[b], kp, abort, p.timeout_ns)) { ok = false; break; }
           tc_fence_after_sync();
           issue_acc(Cfg::kColDK, Cfg::kColDP + 64 * b, aQ + slot * QB, t > 0);     // dK += dS^T Q
           {                                                                          // dQ^T = K^T dS^T
-            uint64_t dA = sdesc_sw128(aK, Cfg::kKVChunk, 1024), dB = sdesc_sw128(adS, Cfg::kKVChunk, 1024);
+            uint64_t dA = sdesc_sw128(aK, Cfg::kKVChunk, 1024);
+            uint64_t dB = sdesc_sw128(adS + b * Cfg::kDsBytes, Cfg::kKVChunk, 1024);
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk) {
               mma_ss(tmem + Cfg::kColS + 64 * b, dA, dB, kIdDq, kk > 0 ? 1u : 0u);
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               asm volatile("" : "+l"(dA), "+l"(dB));
             }
           }
-          mma_commit(&bars->dq_full);
+          mma_commit(&bars->dq_full[b]);
         }
         if (!ok) raise_abort(abort, p.status);
         mma_commit(&bars->mma_drain);
@@ -264,143 +275,160 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     regs_increase<kBwdWorkRegs>();
     // ------------------------------------------------------------ elementwise warps
-    const int wg = warp >> 2;                 // query columns [32 wg, 32 wg + 32) of a tile
+    const int g = warp >> 2;                  // this warpgroup's tiles: t % 2 == g (TMEM buffer g)
     const int wq = warp & 3;
     const int row = wq * 32 + lane;           // TMEM lane: key row (S^T, dP^T, dK, dV) or head column (dQ^T)
     const int key = key0 + row;
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + Cfg::kColS + 64 * g;
+    const uint32_t tDP = tmem + lane_bits + Cfg::kColDP + 64 * g;
     const float sl2 = p.scale_log2;
     const float* L2h = p.L2 + static_cast<size_t>(bh) * p.Nq_pad;
     const float* Drh = p.Dr + static_cast<size_t>(bh) * p.Nq_pad;
-    const uint32_t ds_row = smem_addr(sdS) + row * 128;
+    const uint32_t ds_row = smem_addr(sdS + g * Cfg::kDsBytes) + row * 128;
     const bool leader = (threadIdx.x & 127) == 0;
     bool ok = true;
 
-    // dQ^T of tile t: wait for it, read this warpgroup's 32 queries out of
-    // buffer t % 2, free the buffer, stage the columns in the warpgroup's
-    // half of tile t's ring slot (four 128-byte-swizzled boxes of 32
-    // queries x 32 columns; this thread's column is `row`) and add them into
-    // dQ with TMA reductions.
-    auto readout = [&](int t) {
-      if (!__all_sync(0xffffffffu, wait_bar(&bars->dq_full, t & 1, abort, p.timeout_ns))) {
-        ok = false;
-        return;
-      }
-      tc_fence_after_sync();
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_bits + Cfg::kColS + 64 * (t & 1) + 32 * wg, v);
-      tmem_ld_wait(v);
-      tc_fence_before_sync();
-      bar_arrive(&bars->dq_free);
+    for (int t = g; t < n_tiles && ok; t += 2) {
+      const uint32_t kp = (t >> 1) & 1;       // phase of this tile on the warpgroup's barriers
       const int slot = t % STAGES;
-      uint8_t* stage = wg == 0 ? sQ + slot * QB : sdO + slot * QB;
-      const uint32_t box = smem_addr(stage) + wq * 4096 + ((lane & 3) << 2);
+      const int qbase = (i0 + t) * QR;
+      // this tile's LSE log2(e), fetched while S^T is computed
+      float4 l4v[16];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const uint32_t addr = box + e * 128 + ((((lane >> 2) ^ (e & 7))) << 4);
-        asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(__float_as_uint(__uint_as_float(v[e]) * p.scale))
-                     : "memory");
-      }
-      fence_proxy_async_shared();
-      bar_arrive(&bars->dq_staged[wg]);
-      if (leader) {
-        if (!wait_bar(&bars->dq_staged[wg], t & 1, abort, p.timeout_ns)) {
-          ok = false;
-        } else {
-          const int q0 = (i0 + t) * QR + 32 * wg;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tma_reduce_add_3d(&tm_dq, stage + c * 4096, 32 * c, q0, bh);
-          bulk_commit();
-        }
-      }
-      ok = __all_sync(0xffffffffu, ok);
-    };
-
-    for (int t = 0; t < n_tiles && ok; ++t) {
-      const int b = t & 1;
-      const int qcol0 = (i0 + t) * QR + 32 * wg;   // first query of this warpgroup's columns
-      float4 l4v[8];
-#pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) l4v[e4] = __ldg(reinterpret_cast<const float4*>(L2h + qcol0) + e4);
-      if (!__all_sync(0xffffffffu, wait_bar(&bars->s_full, t & 1, abort, p.timeout_ns))) {
+      for (int e4 = 0; e4 < 16; ++e4) l4v[e4] = __ldg(reinterpret_cast<const float4*>(L2h + qbase) + e4);
+      if (!__all_sync(0xffffffffu, wait_bar(&bars->s_full[g], kp, abort, p.timeout_ns))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       // P^T = exp2(s * scale log2e - LSE log2e) on kept (key, query) pairs
-      float P[32];
-      uint32_t pk[16];
-      {
+      float P[64];
+      uint32_t pk[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
         uint32_t s[32];
-        tmem_ld32(tmem + lane_bits + Cfg::kColS + 64 * b + 32 * wg, s);
+        tmem_ld32(tS + 32 * h, s);
         tmem_ld_wait(s);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l = l4v[e4];
+          const float4 l = l4v[8 * h + e4];
           const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int e = 4 * e4 + u;
-            const int q = qcol0 + e;
+            const int q = qbase + 32 * h + e;
             const bool keep = q < p.Nq && key < p.Nk && (!CAUSAL || key <= q);
-            P[e] = keep ? ex2_approx(fmaf(__uint_as_float(s[e]), sl2, -lv[u])) : 0.f;
+            P[32 * h + e] = keep ? ex2_approx(fmaf(__uint_as_float(s[e]), sl2, -lv[u])) : 0.f;
           }
         }
       }
 #pragma unroll
-      for (int e = 0; e < 16; ++e) pk[e] = pack_x2<F16>(P[2 * e], P[2 * e + 1]);
-      tmem_st16(tmem + lane_bits + Cfg::kColS + 64 * b + 32 * wg, pk);
-      float4 d4v[8];
+      for (int e = 0; e < 32; ++e) pk[e] = pack_x2<F16>(P[2 * e], P[2 * e + 1]);
+      tmem_st32(tS, pk);
+      float4 d4v[16];
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) d4v[e4] = __ldg(reinterpret_cast<const float4*>(Drh + qcol0) + e4);
+      for (int e4 = 0; e4 < 16; ++e4) d4v[e4] = __ldg(reinterpret_cast<const float4*>(Drh + qbase) + e4);
       tmem_st_wait();
       tc_fence_before_sync();
-      bar_arrive(&bars->p_ready);
-      // tile t-2's dQ reductions have had a whole P phase to read their
-      // staging: hand that ring slot back to the producer
+      bar_arrive(&bars->p_ready[g]);
+      // this warpgroup's previous tile's dQ reductions have had a whole P
+      // phase to read their staging: hand that ring slot back to the producer
       if (leader && t >= 2) {
         bulk_wait_read();
         bar_arrive(&bars->q_empty[(t - 2) % STAGES]);
       }
-      // dQ^T(t-1); its completion also means dQ^T(t-1) has read the dS tile
-      if (t >= 1) {
-        readout(t - 1);
-        if (!ok) break;
-      }
 
-      // dS^T = P^T (dP^T - D): to TMEM (A of dK) and to the dS tile (B of dQ^T)
-      {
-        uint32_t g[32];
-        tmem_ld32(tmem + lane_bits + Cfg::kColDP + 64 * b + 32 * wg, g);
-        tmem_ld_wait(g);
+      // dS^T = P^T (dP^T - D): to TMEM (A of dK) and to this warpgroup's dS
+      // tile (B of dQ^T; dQ^T of its previous tile has read it: this
+      // warpgroup waited for that dq_full)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t gv[32];
+        tmem_ld32(tDP + 32 * h, gv);
+        tmem_ld_wait(gv);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 dv = d4v[e4];
+          const float4 dv = d4v[8 * h + e4];
           const float dd[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
           for (int u = 0; u < 4; u += 2) {
             const int e = 4 * e4 + u;
-            const float a = P[e] * (__uint_as_float(g[e]) - dd[u]);
-            const float c = P[e + 1] * (__uint_as_float(g[e + 1]) - dd[u + 1]);
-            pk[e / 2] = pack_x2<F16>(a, c);
+            const float a = P[32 * h + e] * (__uint_as_float(gv[e]) - dd[u]);
+            const float c = P[32 * h + e + 1] * (__uint_as_float(gv[e + 1]) - dd[u + 1]);
+            pk[16 * h + e / 2] = pack_x2<F16>(a, c);
           }
         }
-      }
-      // this key row's 32 queries as four swizzled 16-byte units of its row
+        // this key row's 32 queries of half h as four swizzled 16-byte units
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int unit = 4 * wg + v;
-        st_shared_v4(ds_row + ((unit ^ (row & 7)) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) {
+          const int unit = 4 * h + v;
+          st_shared_v4(ds_row + ((unit ^ (row & 7)) << 4), pk[16 * h + 4 * v], pk[16 * h + 4 * v + 1],
+                       pk[16 * h + 4 * v + 2], pk[16 * h + 4 * v + 3]);
+        }
       }
-      tmem_st16(tmem + lane_bits + Cfg::kColDP + 64 * b + 32 * wg, pk);
+      tmem_st32(tDP, pk);
       tmem_st_wait();
       fence_proxy_async_shared();
       tc_fence_before_sync();
-      bar_arrive(&bars->ds_ready);
+      bar_arrive(&bars->ds_ready[g]);
+
+      // dQ^T(t): read it out (this thread's head column `row`, 64 queries),
+      // free the buffer, stage it in tile t's ring slot (queries 0-31 in
+      // the Q half, 32-63 in the dO half, each as four 128-byte-swizzled
+      // boxes of 32 queries x 32 columns) and add it into dQ with TMA
+      // reductions.  Every MMA of the tile has completed: no MMA reads the
+      // slot any more.
+      if (!__all_sync(0xffffffffu, wait_bar(&bars->dq_full[g], kp, abort, p.timeout_ns))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t v[2][32];
+      tmem_ld32(tS, v[0]);
+      tmem_ld32(tS + 32, v[1]);
+      tmem_ld_wait(v[0]);
+      tmem_ld_wait(v[1]);
+      tc_fence_before_sync();
+      bar_arrive(&bars->dq_free[g]);
+#pragma unroll
+      for (int qh = 0; qh < 2; ++qh) {
+        const uint32_t box = smem_addr((qh == 0 ? sQ : sdO) + slot * QB) + wq * 4096 + ((lane & 3) << 2);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const uint32_t addr = box + e * 128 + (((lane >> 2) ^ (e & 7)) << 4);
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr),
+                       "r"(__float_as_uint(__uint_as_float(v[qh][e]) * p.scale))
+                       : "memory");
+        }
+      }
+      fence_proxy_async_shared();
+      bar_arrive(&bars->dq_staged[g]);
+      if (leader) {
+        if (!wait_bar(&bars->dq_staged[g], kp, abort, p.timeout_ns)) {
+          ok = false;
+        } else {
+#pragma unroll
+          for (int qh = 0; qh < 2; ++qh) {
+            uint8_t* stage = (qh == 0 ? sQ : sdO) + slot * QB;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tma_reduce_add_3d(&tm_dq, stage + c * 4096, 32 * c, qbase + 32 * qh, bh);
+          }
+          bulk_commit();
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
     }
-    if (ok && n_tiles > 0) readout(n_tiles - 1);
     // the last reductions must have read their staging before the CTA exits
     if (leader) bulk_wait_read();
+    // dK and dV are final once every MMA has completed; the warpgroup that
+    // does not own the last tile gets here before that tile's MMAs are done
+    if (ok && n_tiles > 0) {
+      if (!__all_sync(0xffffffffu, wait_bar(&bars->mma_drain, 0, abort, p.timeout_ns)))
+        ok = false;
+      else
+        tc_fence_after_sync();
+    }
 
     // dK = scale dS^T Q and dV = P^T dO for this CTA's keys (zero when no
     // query sees them), as in the one-tile kernel.
@@ -409,7 +437,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       float* dv = p.dV + (static_cast<size_t>(bh) * p.Nk + key) * D;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        const int col = (D / 2) * wg + 32 * c;
+        const int col = (D / 2) * g + 32 * c;
         uint32_t a[32], bb[32];
         if (n_tiles > 0) {
           tmem_ld32(tmem + lane_bits + Cfg::kColDK + col, a);
