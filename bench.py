@@ -603,6 +603,8 @@ def main():
     }
     if not args.no_workloads and args.heads is None:
         line["workloads"] = other_workloads(fa2, dev, w.name, peaks, peak_src)
+        if w.d in (64, 128) and args.dtype == "bf16":
+            line["backward"] = backward_entry(fa2, dev, w, peaks, peak_src)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -690,6 +692,60 @@ def measure_launches(fa2, dev, w, steps=10, warmup=3, num_splits=1):
     del Q, K, V, O, L, flush, workspace
     torch.cuda.empty_cache()
     return statistics.mean(ms), note, extra
+
+
+def backward_entry(fa2, dev, w, peaks, peak_src, steps=5, warmup=3):
+    """The backward pass of the headline workload (pre-pass and tensor-core
+    kernel, one call per step) measured beside the forward: mean CUDA-event
+    time of a call, TFLOP/s at 2.5x the forward's FLOPs, and its roofline."""
+    Qh, Kh, Vh = inputs.workload_inputs(w)
+    Gh = inputs.draw_bf16((w.B, w.H, w.Nq, w.d), w.seed, 3)
+    Q, K, V, G = (t.to(dev) for t in (Qh, Kh, Vh, Gh))
+    del Qh, Kh, Vh, Gh
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev) if backward_l2_note(w)[0] else None
+    with torch.cuda.stream(stream):
+        O, L = fa2.forward(Q, K, V, causal=w.causal, scale=w.scale, stream=stream)
+        dQ = torch.empty(w.B, w.H, w.Nq, w.d, device=dev)
+        dK = torch.empty(w.B, w.H, w.Nk, w.d, device=dev)
+        dV = torch.empty(w.B, w.H, w.Nk, w.d, device=dev)
+        ws = torch.empty(max(fa2.fa2_backward_workspace_bytes(w.B, w.H, w.Nq), 1), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            fa2.backward(Q, K, V, O, L, G, causal=w.causal, scale=w.scale, dq=dQ, dk=dK, dv=dV,
+                         workspace=ws, stream=stream)
+
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(steps):
+            if flush is not None:
+                flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+    if fa2.fa2_device_status(None, reset=True) != fa2.FA2_OK:
+        raise SystemExit("device status error while timing the backward pass")
+    mean_ms = statistics.mean(ms)
+    flops = 2.5 * w.flops
+    tf = flops / (mean_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    algo = algorithmic_bytes_backward(w)
+    hbm_bound = flops / algo < peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    del Q, K, V, G, O, L, dQ, dK, dV, ws, flush
+    torch.cuda.empty_cache()
+    return {"metric": METRIC_BWD, "config": {"workload": w.name, "l2": backward_l2_note(w)[1]},
+            "mean_call_ms": round(mean_ms, 4), "tflops": round(tf, 2), "pct_of_peak": round(100 * tf / peak, 2),
+            "kernels_per_call": 2,
+            "roofline": roofline_entry(hbm_bound, tf, peak, peak_src, peaks,
+                                       recorded_traffic(w.name + ":backward", BWD_KERNEL_SOURCES), flops, algo,
+                                       mean_ms, kernel="fa2dev::fa2_bwd_tc_kernel")}
 
 
 def other_workloads(fa2, dev, headline, peaks, peak_src):
