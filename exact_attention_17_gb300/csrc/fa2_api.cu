@@ -867,6 +867,21 @@ extern "C" int fa2_forward_host(const void* Qh, const void* Kh, const void* Vh, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const long long BH = pr.BH;
   const int n = static_cast<int>(chunks < BH ? chunks : BH);
+  // Head groups weighted min(c + 1, n - c): small groups at both ends shorten
+  // the copy-in before the first computation and the computation and
+  // copy-out after the last copy-in, larger ones in the middle keep each
+  // launch big enough to fill the GPU.  Group c covers heads
+  // [first(c), first(c + 1)), each at least one head.
+  long long wsum = 0;
+  for (int c = 0; c < n; ++c) wsum += (c + 1 < n - c ? c + 1 : n - c);
+  auto first = [&](int c) -> long long {
+    long long w = 0;
+    for (int i = 0; i < c; ++i) w += (i + 1 < n - i ? i + 1 : n - i);
+    long long h = (BH * w + wsum / 2) / wsum;
+    if (h < c) h = c;                         // at least one head per earlier group
+    if (h > BH - (n - c)) h = BH - (n - c);   // at least one head per later group
+    return h;
+  };
   // the pipeline starts after the work already queued on the caller's stream
   bool ok = cudaEventRecord(hp.start, s) == cudaSuccess &&
             cudaStreamWaitEvent(hp.in, hp.start, 0) == cudaSuccess &&
@@ -874,7 +889,7 @@ extern "C" int fa2_forward_host(const void* Qh, const void* Kh, const void* Vh, 
             cudaStreamWaitEvent(hp.out, hp.start, 0) == cudaSuccess;
   const size_t q_head = static_cast<size_t>(Nq) * d, kv_head = static_cast<size_t>(Nk) * d;
   for (int c = 0; c < n && ok; ++c) {
-    const long long h0 = BH * c / n, h1 = BH * (c + 1) / n;
+    const long long h0 = first(c), h1 = c + 1 < n ? first(c + 1) : BH;
     const size_t nh = static_cast<size_t>(h1 - h0), off = static_cast<size_t>(h0);
     const char* qh = static_cast<const char*>(Qh) + off * q_head * 2;
     const char* kh = static_cast<const char*>(Kh) + off * kv_head * 2;

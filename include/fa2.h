@@ -204,8 +204,12 @@ int fa2_forward_splitkv_static(const void *Q, const void *K, const void *V, floa
  * copies in of one group, the computation of another and the copies out of
  * a third run at the same time on three streams of the library's own
  * (created by the first call on a device and kept until the process exits,
- * together with their events).  The result is that of fa2_forward; the
- * heads are independent, so no group needs another's data.
+ * together with their events).  Group c holds about B*H * w_c / sum(w)
+ * heads, w_c = min(c + 1, chunks - c), and at least one: the first and last
+ * groups are small, so little copying precedes the first computation and
+ * little work follows the last copy in.  The result is that of
+ * fa2_forward; the heads are independent, so no group needs another's
+ * data.
  *   Qh, Kh, Vh       host (or any CUDA-addressable) bf16 inputs, layouts as
  *                    above; page-locked memory lets the copies overlap the
  *                    computation, pageable memory gives the same results
