@@ -35,6 +35,15 @@
  * written then) and launch errors.  A kernel that gives up waiting on one of
  * its internal barriers (about 2 s) returns early, leaves its outputs
  * incomplete and sets the device status word, which fa2_device_status reads.
+ *
+ * Kernel variants.  Two environment variables, read at every call, choose
+ * between kernels that compute the same results (up to the rounding order
+ * of their sums) for head dimension 128: FA2_FORWARD_KERNEL = "pair" runs
+ * the forward passes on CTA pairs (two-SM tensor-core MMAs), "single" on
+ * one-CTA kernels; FA2_BACKWARD_KERNEL = "two_tile" runs the backward pass
+ * with two 64-query tiles in flight, "one_tile" with one 128-query tile.
+ * Unset (or any other value) selects the default, the measured faster
+ * choice: "single" and "one_tile".
  */
 #ifndef FA2_H
 #define FA2_H
