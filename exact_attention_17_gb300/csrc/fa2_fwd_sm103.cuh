@@ -122,7 +122,10 @@ struct FwdShape {
                 "register rebalancing exceeds the launch allocation");
   static_assert(kLaunch * kThreads * kCtasPerSm <= 65536, "launch registers exceed the SM");
 };
+// The exponent offset of a row moves only when its scores exceed it by more
+// than this (log2 units), so every P stays <= 2^kRescaleLog2.
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleBound = 256.0f;   // 2^kRescaleLog2
 
 template <int D, int SUBS>
 struct FwdConfig {
@@ -515,71 +518,99 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         if (j > 0) bar_arrive(&bars->kv_empty[(2 * j - 1) % STAGES]);
         bar_arrive(&bars->kv_empty[(2 * j) % STAGES]);
       }
+      // S of this tile, with the masks for keys past the end and keys after
+      // the query under the causal mask
       uint32_t s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
-
-      // masks: keys past the end, and keys after the query under the causal mask
       const int key0 = (t_begin + j) * kKeysPerTile;
       const bool tail = key0 + kKeysPerTile > p.Nk;
       const bool diag = CAUSAL && key0 + kKeysPerTile - 1 > sub_row0;
-      if (tail || diag) {
-        const int lim = CAUSAL ? min(p.Nk, qi + 1) : p.Nk;  // keys [0, lim) are kept
+      auto load_s = [&]() {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (key0 + c * 32 + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
-      }
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+        if (tail || diag) {
+          const int lim = CAUSAL ? min(p.Nk, qi + 1) : p.Nk;  // keys [0, lim) are kept
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (key0 + c * 32 + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
+        }
+      };
 
-      // row max: eight independent 3-input max chains over the 128 scores, then a small tree
+      // Offset decision: the row max (eight independent 3-input max chains
+      // over the 128 scores, then a small tree); the offset moves to it when
+      // it exceeds the current one by more than kRescaleLog2.
+      float m_new = m;
+      float alpha = 1.f;   // correction factor 2^(m - m'): 0 on the first tile, 1 when the offset stays
+      auto decide = [&]() {
 #define FA2_S(f) __uint_as_float(s[(f) >> 5][(f) & 31])
-      float mx8[8];
+        float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = FA2_S(k);
+        for (int k = 0; k < 8; ++k) mx8[k] = FA2_S(k);
 #pragma unroll
-      for (int f = 8; f < 120; f += 16)
+        for (int f = 8; f < 120; f += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], FA2_S(f + k), FA2_S(f + 8 + k));
+          for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], FA2_S(f + k), FA2_S(f + 8 + k));
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], FA2_S(120 + k));
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], FA2_S(120 + k));
 #undef FA2_S
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                             fmaxf(mx8[6], mx8[7]));
-      const float m_cand = fmaxf(m, mx * sl2);
-      const bool move = (j == 0) || (m_cand > m + kRescaleLog2);
-      const float m_new = move ? m_cand : m;
-      // correction factor exp(m - m'): 0 on the first tile, exactly 1 when the offset stays
-      const float alpha = !move ? 1.f : (m == -INFINITY ? 0.f : ex2_approx(m - m_new));
-      const float off = m_new == -INFINITY ? 0.f : m_new;
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
+        const float m_cand = fmaxf(m, mx * sl2);
+        const bool move = (j == 0) || (m_cand > m + kRescaleLog2);
+        m_new = move ? m_cand : m;
+        alpha = !move ? 1.f : (m == -INFINITY ? 0.f : ex2_approx(m - m_new));
+      };
 
       // P = 2^(s * scale*log2e - offset), packed pairwise; row sum in four packed accumulators
-      const float2 c2 = make_float2(sl2, sl2);
-      const float2 o2 = make_float2(-off, -off);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
       uint32_t pk[2][32];
+      float rs;
+      auto exps = [&]() {
+        const float off = m_new == -INFINITY ? 0.f : m_new;
+        const float2 c2 = make_float2(sl2, sl2);
+        const float2 o2 = make_float2(-off, -off);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 t = __ffma2_rn(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), c2, o2);
-          const float2 pe = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-          acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], pe);
-          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_x2<F16>(pe.x, pe.y);
+          for (int e = 0; e < 32; e += 2) {
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), c2, o2);
+            const float2 pe = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], pe);
+            pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_x2<F16>(pe.x, pe.y);
+          }
         }
-        // the first half of P goes to TMEM while the second half is computed
-        if (c == 1) tmem_st32(tS, pk[0]);
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+        const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a = __fadd2_rn(a01, a23);
+        rs = a.x + a.y;
+      };
+
+      // Once the offset is finite, the exponentials go first with the
+      // offset as it stands: the offset can only have to move when some
+      // term exceeds 2^kRescaleLog2, and then the row sum does too.  Only
+      // then (rarely, once the first tiles have set the offset) is the row
+      // max taken, from S read again (P is not yet stored over it), and the
+      // exponentials redone with the offset it decides.  Rows that do not
+      // move redo the same arithmetic, so every row's offset and P are
+      // those of taking the max first, but for a max within rounding of the
+      // bound.
+      load_s();
+      const bool max_first = __any_sync(0xffffffffu, m == -INFINITY);
+      if (max_first) decide();
+      exps();
+      if (!max_first && __any_sync(0xffffffffu, rs > kRescaleBound)) {
+        load_s();
+        decide();
+        exps();
       }
-      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
-      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
-      const float2 a = __fadd2_rn(a01, a23);
-      const float rs = a.x + a.y;
+      tmem_st32(tS, pk[0]);
+      tmem_st32(tS + 32, pk[1]);
       l = l * alpha + rs;
       m = m_new;
-      tmem_st32(tS + 32, pk[1]);
 
       // correction of the running output when some row of this warp moved its offset
       // (single-buffered order: the wait for S(j) above already follows P(j-1) V)
