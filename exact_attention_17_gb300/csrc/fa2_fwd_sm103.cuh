@@ -155,6 +155,13 @@ struct FwdConfig {
   // single-buffered issue order S(j+1) follows P(j) V, so the softmax's wait
   // for S(j+1) already orders its rescale of O after P(j) V.
   static constexpr bool kOutDoneLast = !kDoubleS;
+  // With a ring of four or more slots the issuing thread waits on named
+  // (hardware) barriers instead of polling mbarriers: an mbarrier check costs
+  // it about 100 cycles while the tensor pipe keeps shared memory busy, and
+  // the pipe idles meanwhile.  A watcher warp waits for the K/V copies and
+  // joins the first of them (the two-slot ring and the double-buffered order
+  // keep their mbarriers).
+  static constexpr bool kNamedP = !kDoubleS && kStages >= 4;
   // TMEM columns: S buffers (128 fp32 columns each), then O of each sub-tile (D).
   static constexpr uint32_t kColsO0 = (kDoubleS ? 2 : SUBS) * 128;
   static constexpr uint32_t kColsO1 = kColsO0 + D;
@@ -164,6 +171,24 @@ struct FwdConfig {
   static constexpr uint32_t kSmemBytes = kSmemData + 1024 /*align*/ + 1024 /*barriers*/;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
+
+// Named barriers of the forward kernels (0 is __syncthreads).  kBarP0: P_0(j)
+// written (4 softmax warps) and V_j, K_(j+1) landed (the watcher warp), for
+// the issuing warp; kBarP1: P_1(j) written (4 softmax warps), for the issuing
+// warp.  Every participant waits at every phase, in order, also after an
+// abort, so that no wait on them is left without its arrivals: a named
+// barrier has no phase number, so an arrival that ran a phase ahead would
+// be counted in the open one.  (The softmax warps lose nothing by waiting:
+// their next S cannot be ready before the issuing warp has passed.)
+constexpr int kBarP0 = 1;
+constexpr int kBarP1 = 2;
+constexpr int kBarP0Count = kRowsPerSub + 64;   // softmax warpgroup 0, issuing warp, watcher warp
+constexpr int kBarP0Idle = 64;                  // issuing and watcher warps (sub-tile 0 done)
+constexpr int kBarP1Count = kRowsPerSub + 32;   // softmax warpgroup 1, issuing warp
+
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 template <int STAGES>
 struct alignas(8) FwdBarriers {
@@ -355,6 +380,95 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         for (int k = max(0, issued - STAGES); k < issued; ++k)
           wait_bar(&bars->kv_full[k % STAGES], (k / STAGES) & 1, &never, p.timeout_ns);
       }
+    } else if (warp == kWarpMma + 1 && Cfg::kNamedP) {
+      // ------------------------------------------------------------ K/V watcher
+      // Tile j's first named-barrier phase also stands for V_j and K_(j+1)
+      // having landed.  After an abort the waits are skipped, not the phases.
+      bool ok = true;
+      for (int j = 0; j < nmax; ++j) {
+        if (lane == 0 && ok) {
+          const int iv = 2 * j + 1, ik = 2 * j + 2;
+          ok = wait_bar(&bars->kv_full[iv % STAGES], (iv / STAGES) & 1, abort, p.timeout_ns);
+          if (ok && j + 1 < nmax)
+            ok = wait_bar(&bars->kv_full[ik % STAGES], (ik / STAGES) & 1, abort, p.timeout_ns);
+          if (!ok) raise_abort(abort, p.status);
+        }
+        __syncwarp();
+        named_sync(kBarP0, j < n0 ? kBarP0Count : kBarP0Idle);
+      }
+    } else if (warp == kWarpMma && Cfg::kNamedP) {
+      // ------------------------------------------------------------ MMA issuer (named barriers)
+      // The whole warp takes part in the named barriers; lane 0 issues every
+      // MMA and every commit.  After an abort the MMAs still go out (on
+      // whatever the buffers hold: the outputs are not written then), so that
+      // every phase of the named barriers is passed.
+      constexpr uint32_t kIdescS = idesc_f32acc(kRowsPerSub, kKeysPerTile, false, false, F16);
+      constexpr uint32_t kIdescO = idesc_f32acc(kRowsPerSub, D, false, true, F16);
+      const uint32_t sQaddr = smem_addr(sQ);
+      const uint32_t sKVaddr = smem_addr(sKV);
+      auto issue_s = [&](int sub, int slot) {
+        uint64_t da = sdesc_sw128(sQaddr + sub * TILE, 16, 1024);
+        uint64_t db = sdesc_sw128(sKVaddr + slot * TILE, 16, 1024);
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          mma_ss(tmem + sub * 128, da, db, kIdescS, kk > 0 ? 1u : 0u);
+          const uint32_t step = ((kk & 3) == 3 ? kChunkBytes - 3 * 32 : 32) >> 4;
+          da += step;
+          db += step;
+          asm volatile("" : "+l"(da), "+l"(db));
+        }
+      };
+      auto issue_pv = [&](int sub, int slot, bool acc) {
+        uint64_t dv = sdesc_sw128(sKVaddr + slot * TILE, kChunkBytes, 1024);
+        const uint32_t o = tmem + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
+        const uint32_t a = tmem + sub * 128;
+  #pragma unroll
+        for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
+          mma_ts(o, a + kk * 8, dv, kIdescO, (acc || kk > 0) ? 1u : 0u);
+          dv += (16 * 128) >> 4;
+          asm volatile("" : "+l"(dv));
+        }
+      };
+      if (lane == 0 && nmax > 0) {
+        const bool ok = wait_bar(&bars->q_full, 0, abort, p.timeout_ns) &&
+                        wait_bar(&bars->kv_full[0], 0, abort, p.timeout_ns);
+        if (!ok) raise_abort(abort, p.status);
+        tc_fence_after_sync();
+        if (n0 > 0) { issue_s(0, 0); mma_commit(&bars->s_full[0]); }
+        if (n1 > 0) { issue_s(1, 0); mma_commit(&bars->s_full[1]); }
+      }
+      __syncwarp();
+      for (int j = 0; j < nmax; ++j) {
+        const int slot_v = (2 * j + 1) % STAGES, slot_k = (2 * j + 2) % STAGES;
+        const bool next = j + 1 < nmax;
+        named_sync(kBarP0, j < n0 ? kBarP0Count : kBarP0Idle);   // P_0(j); V_j, K_(j+1) landed
+        if (lane == 0) {
+          tc_fence_after_sync();
+          if (j < n0) {
+            issue_pv(0, slot_v, j > 0);
+            if (j + 1 == n0) mma_commit(&bars->o_done[0]);
+          }
+          if (next && j + 1 < n0) { issue_s(0, slot_k); mma_commit(&bars->s_full[0]); }
+        }
+        __syncwarp();
+        if (j < n1) {
+          named_sync(kBarP1, kBarP1Count);                      // P_1(j)
+          if (lane == 0) {
+            tc_fence_after_sync();
+            issue_pv(1, slot_v, j > 0);
+            if (j + 1 == n1) mma_commit(&bars->o_done[1]);
+            if (next && j + 1 < n1) { issue_s(1, slot_k); mma_commit(&bars->s_full[1]); }
+          }
+          __syncwarp();
+        }
+      }
+      if (lane == 0 && nmax > 0) {
+        // Every MMA must be complete before TMEM is released.
+        mma_commit(&bars->mma_drain);
+        volatile int never = 0;
+        wait_bar(&bars->mma_drain, 0, &never, p.timeout_ns);
+      }
+      __syncwarp();
     } else if (warp == kWarpMma) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0 && nmax > 0) {
@@ -502,6 +616,7 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
     float m = -INFINITY;  // running max (log2 domain) used as the exponent offset
     float l = 0.f;        // running sum of 2^(t - m)
     bool ok = true;
+    int announced = 0;    // tiles whose P was announced to the issuing warp
     for (int j = 0; j < n_tiles; ++j) {
       // all lanes must agree before the warp-collective TMEM accesses
       // S of this tile: the sub-tile's buffer, or buffer j % 2 when double-buffered
@@ -634,8 +749,20 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      bar_arrive(&bars->p_ready[Cfg::kDoubleS ? (j & 1) : sub]);
+      if constexpr (Cfg::kNamedP) {
+        __syncwarp();
+        named_sync(sub == 0 ? kBarP0 : kBarP1, sub == 0 ? kBarP0Count : kBarP1Count);
+      } else {
+        bar_arrive(&bars->p_ready[Cfg::kDoubleS ? (j & 1) : sub]);
+      }
+      announced = j + 1;
       if (!ok) break;
+    }
+    if constexpr (Cfg::kNamedP) {
+      // after an abort: the remaining phases, in step with the issuing warp
+      __syncwarp();
+      for (int j = announced; j < n_tiles; ++j)
+        named_sync(sub == 0 ? kBarP0 : kBarP1, sub == 0 ? kBarP0Count : kBarP1Count);
     }
 
     // Outputs of this row: the final ones, or this key range's partial ones.
