@@ -729,12 +729,21 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
 
       // correction of the running output when some row of this warp moved its offset
       // (single-buffered order: the wait for S(j) above already follows P(j-1) V)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!Cfg::kOutDoneLast &&
-            !__all_sync(0xffffffffu, wait_bar(&bars->o_done[sub], (j - 1) & 1, abort, p.timeout_ns))) {
-          ok = false;
-        }
-        else {
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      // Double-buffered order, O announced after every P V: the wait for
+      // P(j-1) V is taken before a rescale, and at the last tile in any case.
+      // When S(j) has completed, P(j-2) V has too (it was issued first), so
+      // o_done is at most one phase behind the one waited for here; after
+      // the last tile's wait it is at most one behind the epilogue's.  (A
+      // parity wait cannot tell a phase from the one two before it: without
+      // the last tile's wait the epilogue could read O before P(n-2) V and
+      // P(n-1) V have completed.)
+      if (!Cfg::kOutDoneLast && j > 0 && (rescale || j == n_tiles - 1) &&
+          !__all_sync(0xffffffffu, wait_bar(&bars->o_done[sub], (j - 1) & 1, abort, p.timeout_ns))) {
+        ok = false;
+      }
+      if (rescale && ok) {
+        {
           tc_fence_after_sync();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {

@@ -112,11 +112,14 @@ class NamedSim(Sim):
         for g in range(2 * nmax):
             slot, r = g % S, g // S
             if r > 0:
-                while not self.slot_empty[slot].done(r - 1):
-                    if self.abort:
-                        return
+                # (after an abort the issuing warp's commits may run ahead of
+                # this wait; the kernel's producer then stops at its next
+                # check of the abort flag, or copies data nothing reads)
+                while not self.abort and not self.slot_empty[slot].done(r - 1):
                     self.tick("producer")
                     yield
+            if self.abort:
+                return
             self.slot_full[slot].arrive(tx_bytes=self.TILE)
             self.tma_load(self.slot_full[slot], slot, g)
             self.tick("producer")
@@ -314,3 +317,4 @@ def test_model_catches_a_count_without_the_watcher():
     class Short(NamedSim):
         p0_count = 128 + 32
     assert _fails(Short, [(4, 3, 3)], abort=False)
+

@@ -19,8 +19,12 @@ in random order).  It fails on:
 * a deadlock.
 
 The model mirrors the producer, issuer and softmax loops of the kernel in
-exact_attention_17_gb300/csrc/fa2_fwd_sm103.cuh; a change to that protocol
-must be made here too.
+exact_attention_17_gb300/csrc/fa2_fwd_sm103.cuh where the issuing thread
+polls mbarriers: the single-buffered two-slot ring (Sim) and the
+double-buffered order of head dimension 256 (DoubleSSim).  With a ring of
+four or more slots the issuing warp waits on named barriers instead; that
+form is modelled in test_named_barrier_protocol.py on top of this one.  A
+change to the kernel's protocol must be made in the models too.
 """
 import random
 
@@ -55,10 +59,15 @@ class MBarrier:
         self._maybe_complete()
 
     def done(self, phase):
-        """Has phase number `phase` completed?  Checks the parity hazard."""
+        """Has phase number `phase` completed?  Checks the parity hazard: a
+        parity wait cannot tell phase p from phase p - 2 or p + 2, so the
+        barrier must be within one phase of the waiter's, on either side."""
         if self.completed > phase + 1:
             raise ProtocolError(f"{self.name}: waiter for phase {phase} sees {self.completed} "
                                 "completed phases (parity aliasing)")
+        if self.completed < phase:
+            raise ProtocolError(f"{self.name}: waiter for phase {phase} sees only {self.completed} "
+                                "completed phases (its parity wait would pass at once)")
         return self.completed == phase + 1
 
 
@@ -182,6 +191,9 @@ class Sim:
 
     # O of a sub-tile is announced (o_done) only after its last P V.
     out_done_last = True
+    # With O announced after every P V: the softmax waits for P(j-1) V at the
+    # last tile (off only in the test that checks the model rejects that).
+    last_tile_wait = True
 
     def o_done_phase(self, n):
         """Phase of o_done that announces the last P V of an n-tile sub-tile."""
@@ -290,11 +302,15 @@ class Sim:
                 raise ProtocolError(f"softmax{sub}({j}) reads TMEM holding {self.tmem_s[buf]}")
             yield
             self.tmem_s[buf] = ("P", j)
-            if j > 0 and self.rng.random() < self.rescale_prob:
-                # (with O announced only at the end, the wait for S(j) above
-                # must already order the rescale after P(j-1) V)
-                while not self.out_done_last and not self.o_done[sub].done(j - 1):
+            rescale = j > 0 and self.rng.random() < self.rescale_prob
+            # (with O announced only at the end, the wait for S(j) above
+            # must already order the rescale after P(j-1) V; with O announced
+            # after every P V the wait for P(j-1) V is also taken at the last
+            # tile, so that the epilogue's parity wait is not two phases ahead)
+            if not self.out_done_last and j > 0 and (rescale or (j == n - 1 and self.last_tile_wait)):
+                while not self.o_done[sub].done(j - 1):
                     yield
+            if rescale:
                 # the rescale reads and writes O: it must hold tiles 0..j-1 exactly
                 if self.o_tiles[sub] != j - 1:
                     raise ProtocolError(f"rescale at tile {j} sees O holding tile {self.o_tiles[sub]}")
@@ -405,6 +421,23 @@ class DoubleSSim(Sim):
 def test_double_s_protocol_random_interleavings(n0):
     for seed in range(60):
         DoubleSSim(2, n0, seed).run()
+
+
+def test_model_catches_epilogue_wait_two_phases_ahead():
+    """With S double-buffered and O announced after every P V, the softmax can
+    finish the last tile before P(n-2) V has completed; the epilogue's parity
+    wait for P(n-1) V would then pass at once.  The wait for P(n-2) V at the
+    last tile prevents it; the model must reject its absence."""
+
+    class NoLastWait(DoubleSSim):
+        last_tile_wait = False
+    failures = 0
+    for seed in range(100):
+        try:
+            NoLastWait(2, 3, seed, rescale_prob=0.0).run()
+        except ProtocolError:
+            failures += 1
+    assert failures > 0
 
 
 def test_model_catches_single_p_ready_with_double_s():
