@@ -186,6 +186,17 @@ constexpr int kBarP0Count = kRowsPerSub + 64;   // softmax warpgroup 0, issuing 
 constexpr int kBarP0Idle = 64;                  // issuing and watcher warps (sub-tile 0 done)
 constexpr int kBarP1Count = kRowsPerSub + 32;   // softmax warpgroup 1, issuing warp
 
+// Ties 32 registers written by a tcgen05.ld to a preceding tcgen05.wait::ld
+// (asm volatile statements keep their order): no instruction is emitted.
+__device__ __forceinline__ void regs_after_wait(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                 "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                 "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -642,8 +653,11 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
       auto load_s = [&]() {
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+        // one wait covers the four loads; the others' registers are only
+        // tied to it, so that nothing reads them before it
+        tmem_ld_wait(s[0]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+        for (int c = 1; c < 4; ++c) regs_after_wait(s[c]);
         if (tail || diag) {
           const int lim = CAUSAL ? min(p.Nk, qi + 1) : p.Nk;  // keys [0, lim) are kept
 #pragma unroll
@@ -715,12 +729,14 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
       // bound.
       load_s();
       const bool max_first = __any_sync(0xffffffffu, m == -INFINITY);
+      bool decided = max_first;   // (otherwise alpha is 1 on every lane)
       if (max_first) decide();
       exps();
       if (!max_first && __any_sync(0xffffffffu, rs > kRescaleBound)) {
         load_s();
         decide();
         exps();
+        decided = true;
       }
       tmem_st32(tS, pk[0]);
       tmem_st32(tS + 32, pk[1]);
@@ -729,7 +745,7 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
 
       // correction of the running output when some row of this warp moved its offset
       // (single-buffered order: the wait for S(j) above already follows P(j-1) V)
-      const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      const bool rescale = decided && j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
       // Double-buffered order, O announced after every P V: the wait for
       // P(j-1) V is taken before a rescale, and at the last tile in any case.
       // When S(j) has completed, P(j-2) V has too (it was issued first), so
