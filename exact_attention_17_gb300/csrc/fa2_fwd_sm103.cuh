@@ -197,6 +197,30 @@ __device__ __forceinline__ void regs_after_wait(uint32_t (&r)[32]) {
                  "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
+// MMAs from descriptors given as 32-bit halves: only the low word (its
+// 14-bit start-address field) steps from one K step to the next, so one
+// 32-bit add per step instead of a 64-bit one.
+__device__ __forceinline__ void mma_ss_halves(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                              uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_halves(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -418,26 +442,30 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
       const uint32_t sQaddr = smem_addr(sQ);
       const uint32_t sKVaddr = smem_addr(sKV);
       auto issue_s = [&](int sub, int slot) {
-        uint64_t da = sdesc_sw128(sQaddr + sub * TILE, 16, 1024);
-        uint64_t db = sdesc_sw128(sKVaddr + slot * TILE, 16, 1024);
+        const uint64_t da = sdesc_sw128(sQaddr + sub * TILE, 16, 1024);
+        const uint64_t db = sdesc_sw128(sKVaddr + slot * TILE, 16, 1024);
+        uint32_t a_lo = static_cast<uint32_t>(da), b_lo = static_cast<uint32_t>(db);
+        const uint32_t a_hi = static_cast<uint32_t>(da >> 32), b_hi = static_cast<uint32_t>(db >> 32);
   #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          mma_ss(tmem + sub * 128, da, db, kIdescS, kk > 0 ? 1u : 0u);
+          mma_ss_halves(tmem + sub * 128, a_lo, a_hi, b_lo, b_hi, kIdescS, kk > 0 ? 1u : 0u);
           const uint32_t step = ((kk & 3) == 3 ? kChunkBytes - 3 * 32 : 32) >> 4;
-          da += step;
-          db += step;
-          asm volatile("" : "+l"(da), "+l"(db));
+          a_lo += step;
+          b_lo += step;
+          asm volatile("" : "+r"(a_lo), "+r"(b_lo));
         }
       };
       auto issue_pv = [&](int sub, int slot, bool acc) {
-        uint64_t dv = sdesc_sw128(sKVaddr + slot * TILE, kChunkBytes, 1024);
+        const uint64_t dv = sdesc_sw128(sKVaddr + slot * TILE, kChunkBytes, 1024);
+        uint32_t v_lo = static_cast<uint32_t>(dv);
+        const uint32_t v_hi = static_cast<uint32_t>(dv >> 32);
         const uint32_t o = tmem + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
         const uint32_t a = tmem + sub * 128;
   #pragma unroll
         for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
-          mma_ts(o, a + kk * 8, dv, kIdescO, (acc || kk > 0) ? 1u : 0u);
-          dv += (16 * 128) >> 4;
-          asm volatile("" : "+l"(dv));
+          mma_ts_halves(o, a + kk * 8, v_lo, v_hi, kIdescO, (acc || kk > 0) ? 1u : 0u);
+          v_lo += (16 * 128) >> 4;
+          asm volatile("" : "+r"(v_lo));
         }
       };
       if (lane == 0 && nmax > 0) {
