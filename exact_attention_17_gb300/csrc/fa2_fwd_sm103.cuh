@@ -524,28 +524,32 @@ __global__ void __launch_bounds__(FwdShape<SUBS>::kThreads, FwdShape<SUBS>::kCta
         // S_sub = Q_sub K^T into S buffer `buf` (by default the sub-tile's
         // own): K-major A and B, K = D in steps of 16.
         auto issue_s = [&](int sub, int slot, int buf) {
-          uint64_t da = sdesc_sw128(sQaddr + sub * TILE, 16, 1024);
-          uint64_t db = sdesc_sw128(sKVaddr + slot * TILE, 16, 1024);
+          const uint64_t da = sdesc_sw128(sQaddr + sub * TILE, 16, 1024);
+          const uint64_t db = sdesc_sw128(sKVaddr + slot * TILE, 16, 1024);
+          uint32_t a_lo = static_cast<uint32_t>(da), b_lo = static_cast<uint32_t>(db);
+          const uint32_t a_hi = static_cast<uint32_t>(da >> 32), b_hi = static_cast<uint32_t>(db >> 32);
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            mma_ss(tmem + buf * 128, da, db, kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss_halves(tmem + buf * 128, a_lo, a_hi, b_lo, b_hi, kIdescS, kk > 0 ? 1u : 0u);
             // next K step: 32 bytes within a 128-byte swizzle atom, else the next 64-column chunk
             const uint32_t step = ((kk & 3) == 3 ? kChunkBytes - 3 * 32 : 32) >> 4;
-            da += step;
-            db += step;
-            asm volatile("" : "+l"(da), "+l"(db));   // one step at a time: keeps two registers live
+            a_lo += step;
+            b_lo += step;
+            asm volatile("" : "+r"(a_lo), "+r"(b_lo));   // one step at a time: keeps two registers live
           }
         };
         // O_sub (+)= P_sub V : P from TMEM S buffer `buf` (bf16, 2 per column), V MN-major.
         auto issue_pv = [&](int sub, int slot, bool acc, int buf) {
-          uint64_t dv = sdesc_sw128(sKVaddr + slot * TILE, kChunkBytes, 1024);
+          const uint64_t dv = sdesc_sw128(sKVaddr + slot * TILE, kChunkBytes, 1024);
+          uint32_t v_lo = static_cast<uint32_t>(dv);
+          const uint32_t v_hi = static_cast<uint32_t>(dv >> 32);
           const uint32_t o = tmem + (sub == 0 ? Cfg::kColsO0 : Cfg::kColsO1);
           const uint32_t a = tmem + buf * 128;
   #pragma unroll
           for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
-            mma_ts(o, a + kk * 8, dv, kIdescO, (acc || kk > 0) ? 1u : 0u);
-            dv += (16 * 128) >> 4;   // next 16 keys of V
-            asm volatile("" : "+l"(dv));
+            mma_ts_halves(o, a + kk * 8, v_lo, v_hi, kIdescO, (acc || kk > 0) ? 1u : 0u);
+            v_lo += (16 * 128) >> 4;   // next 16 keys of V
+            asm volatile("" : "+r"(v_lo));
           }
         };
 
