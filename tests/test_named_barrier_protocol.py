@@ -36,7 +36,6 @@ an abort without passing its remaining phases, a watcher that stops at an
 abort, and a count that leaves out the watcher -- must each end in a
 reported error.
 """
-import random
 
 import pytest
 
