@@ -142,3 +142,20 @@ def test_splitkv_workspace_errors(dev):
     assert fa2.fa2_forward_splitkv(*bad, ws.data_ptr(), need, None) == fa2.FA2_ERR_SHAPE
     assert fa2.fa2_forward_splitkv(*args, ws.data_ptr(), need, None) == fa2.FA2_OK
     torch.cuda.synchronize()
+
+
+# Causal key ranges one key tile long on grids large enough for two query
+# sub-tiles per CTA: ranges that only a CTA's second sub-tile reaches (its
+# first has no kept key there) and ranges past both, on the kernel form whose
+# issuing warp waits on named barriers.
+@pytest.mark.parametrize("d", [64, 128])
+def test_splitkv_two_subtile_grid_with_ranges_only_the_second_subtile_reaches(dev, d):
+    B, H, N, splits = 1, 4, 4096, 32
+    assert (N + 255) // 256 * B * H * splits >= 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    Q, K, V = inputs.make_qkv(B, H, N, N, d, seed=97 + d)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    O, L = fa2.forward(Q.to(dev), K.to(dev), V.to(dev), causal=True, scale=scale, num_splits=splits)
+    torch.cuda.synchronize()
+    assert fa2.fa2_device_status(None) == fa2.FA2_OK
+    Or, Lr = oracle.attention(*bits(Q, K, V), True, scale)
+    check(O, L, Or, Lr, f"split-KV two-sub-tile grid d={d}")
